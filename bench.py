@@ -1,0 +1,489 @@
+"""Throughput of one continuous-batching attention step on the GPU.
+
+A step is the whole hot path over one batch: copy-on-write block copies (when
+the workload has any), the KV scatter, and ragged causal paged attention
+(split-KV decode + combine for single-token rows, the prefill kernel for the
+rest).  The headline workload is the pure-decode batch: 256 sequences x 1 new
+token, history uniform in [512, 4096], 32/32 heads of 128 dims, block size
+16, a 70,000-block pool; its metric is the KV bytes the step must read per
+second.  Prefill (16 ragged prompts, 8192 tokens, 32/8 heads) and the mixed
+step (240 decodes + two 3976-token chunks) are reported as secondary
+measurements.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica (the path has no
+collective); rank 0 prints one JSON line.  ``--impl reference`` times the CPU
+oracle on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode KV-read GB/s"
+BASELINE_METRIC = "decode KV-read GB/s, prefill TFLOP/s, mixed-batch attn tokens/s (1×GB300)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+
+def kv_bytes(seq_lens, num_kv_heads, head_dim, itemsize=2):
+    """K and V bytes a step must read: every live key of every sequence, once."""
+    return int(np.sum(np.asarray(seq_lens, dtype=np.int64))) * 2 * num_kv_heads * head_dim * itemsize
+
+
+def decode_kernel_bytes(lay, rows):
+    """Algorithmic bytes of the decode kernel for sequences ``rows``: K/V of every
+    live key, the query and output rows, and the block-table entries it reads."""
+    seq = lay.seq_lens[rows].astype(np.int64)
+    kv = kv_bytes(seq, lay.num_kv_heads, lay.head_dim)
+    qo = 2 * len(rows) * lay.num_q_heads * lay.head_dim * 2
+    tables = int(np.sum(-(-seq // lay.block_size))) * 4
+    return kv + qo + tables
+
+
+def attention_flops(lay, rows):
+    """4 * D FLOPs per visible (query head, key) pair (q.k and p.v)."""
+    q = lay.query_lens[rows].astype(np.int64)
+    c = (lay.seq_lens[rows] - lay.query_lens[rows]).astype(np.int64)
+    pairs = int(np.sum(q * c + q * (q + 1) // 2))
+    return 4 * lay.head_dim * lay.num_q_heads * pairs
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "src": "measured"}
+    return {"hbm": FALLBACK_HBM_GBS, "bf16": FALLBACK_BF16_TFLOPS,
+            "bf16_sustained": FALLBACK_BF16_TFLOPS, "src": "fallback"}
+
+
+def source_digest(*names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_133_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel, workload, digest):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    for e in json.load(open(p)):
+        if e.get("kernel") == kernel and e.get("workload") == workload and e.get("source") == digest:
+            return float(e["dram_bytes_per_launch"])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        loaded = [x for x in sm if x > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+
+class Step:
+    """Device-resident inputs of one workload and the calls of one step."""
+
+    def __init__(self, lay, dev, seed=0):
+        import torch
+        import paged_kv_cache_133_gb300 as pa
+        self.pa, self.torch, self.lay, self.dev = pa, torch, lay, dev
+        self.g = workloads.make_tensors(lay, seed=seed, device=dev)
+        self.md = {
+            "qsl": torch.from_numpy(lay.query_start_loc).to(dev),
+            "seq_lens": torch.from_numpy(lay.seq_lens).to(dev),
+            "bt": torch.from_numpy(lay.block_tables).to(dev),
+            "slots": torch.from_numpy(lay.slot_mapping).to(dev),
+            "pairs": torch.from_numpy(np.ascontiguousarray(lay.cow_pairs, np.int32)).to(dev),
+        }
+        self.out = torch.empty_like(self.g["q"])
+        need = pa.workspace_size(lay.num_decode_seqs, lay.num_q_heads, lay.num_kv_heads,
+                                 lay.head_dim, lay.max_seq_len)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(self, attn_events=None, g=None, md=None):
+        pa, lay = self.pa, self.lay
+        g = g or self.g
+        md = md or self.md
+        if len(lay.cow_pairs):
+            pa.copy_blocks(g["k_cache"], g["v_cache"], md["pairs"], err=self.err)
+        pa.write_kv(g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"], err=self.err)
+        if attn_events is not None:
+            attn_events[0].record()
+        pa.attention(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"], md["bt"],
+                     num_decode_seqs=lay.num_decode_seqs, max_query_len=lay.max_query_len,
+                     max_seq_len=lay.max_seq_len, scale=lay.scale, out=self.out,
+                     workspace=self.ws, err=self.err)
+        if attn_events is not None:
+            attn_events[1].record()
+
+
+def _barrier(dist_on):
+    if dist_on:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, dist_on, dev):
+    if not dist_on:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_device(step, steps, warmup, dist_on, clocks=None):
+    """Device time per step (ms) and mean attention-call time (ms) over the timed steps."""
+    torch = step.torch
+    for _ in range(warmup):
+        step.run()
+    _barrier(dist_on)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    launches0 = step.pa.kernel_launches()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ctx = clocks if clocks is not None else _Null()
+    with ctx:
+        start.record()
+        for i in range(steps):
+            step.run(attn_events=ev[i])
+        end.record()
+        torch.cuda.synchronize()
+    launches = step.pa.kernel_launches() - launches0
+    _barrier(dist_on)
+    total = start.elapsed_time(end)
+    attn = sum(a.elapsed_time(b) for a, b in ev) / steps
+    return total / steps, attn, launches
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def time_e2e(step, steps, warmup, dist_on):
+    """Per-step time with the step's inputs copied in from pinned host memory
+    and the output read back, all inside the timed region."""
+    torch = step.torch
+    lay = step.lay
+    host = {k: step.g[k].cpu().pin_memory() for k in ("q", "k", "v")}
+    for k in ("qsl", "seq_lens", "bt", "slots", "pairs"):
+        host[k] = step.md[k].cpu().pin_memory()
+    dev_in = {k: torch.empty_like(step.g[k]) for k in ("q", "k", "v")}
+    dev_md = {k: torch.empty_like(step.md[k]) for k in step.md}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for k in ("q", "k", "v"):
+            dev_in[k].copy_(host[k], non_blocking=True)
+        for k in dev_md:
+            dev_md[k].copy_(host[k], non_blocking=True)
+        g = {"q": dev_in["q"], "k": dev_in["k"], "v": dev_in["v"],
+             "k_cache": step.g["k_cache"], "v_cache": step.g["v_cache"]}
+        step.run(g=g, md=dev_md)
+        out_host.copy_(step.out, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    _barrier(dist_on)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    _barrier(dist_on)
+    return s.elapsed_time(e) / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+
+def sample_layout(lay, seqs):
+    """A layout holding only sequences ``seqs`` of ``lay`` (same lengths and heads),
+    with a pool sized exactly for them."""
+    cached = lay.cached_lens[seqs]
+    queries = lay.query_lens[seqs]
+    nb = int(np.sum(-(-lay.seq_lens[seqs].astype(np.int64) // lay.block_size)))
+    return workloads.custom_layout(lay.name + "-sample", cached, queries, lay.num_q_heads,
+                                   lay.num_kv_heads, lay.head_dim, lay.block_size, nb, 77)
+
+
+def oracle_step_seconds(sub, seed=0):
+    """Wall time of the oracle's scatter + attention on a sample layout (CPU)."""
+    import torch
+    from oracle import attention as ref
+    ts = workloads.make_tensors(sub, seed=seed)
+    f = {k: v.to(torch.float64).numpy() for k, v in ts.items()}
+    t0 = time.perf_counter()
+    kc, vc = ref.write_kv(f["k_cache"], f["v_cache"], f["k"], f["v"], sub.slot_mapping,
+                          sub.block_size)
+    ref.attention(f["q"], kc, vc, sub.query_start_loc, sub.seq_lens, sub.block_tables,
+                  sub.block_size, sub.scale, sub.num_kv_heads)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(lay, budget_s=12.0):
+    """Oracle GB/s on a bounded sample of the decode workload (first sequences)."""
+    seqs, elapsed, nbytes = [], 0.0, 0
+    i = 0
+    while elapsed < budget_s and i < lay.num_seqs:
+        batch = list(range(i, min(lay.num_seqs, i + 4)))
+        sub = sample_layout(lay, np.array(batch))
+        elapsed += oracle_step_seconds(sub, seed=i)
+        nbytes += kv_bytes(sub.seq_lens, sub.num_kv_heads, sub.head_dim)
+        seqs += batch
+        i += 4
+    return {"value": nbytes / elapsed / 1e9, "unit": "GB/s", "cores": cpu_cores(),
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle (scatter + attention) on the first {len(seqs)} of "
+                      f"{lay.num_seqs} decode sequences, {elapsed:.1f} s; BLAS threads default"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    lay = workloads.config_layout(2, args.seed)
+    per = 2
+    rng = np.random.default_rng(args.seed)
+    times, nbytes = [], []
+    for it in range(args.warmup + args.steps):
+        seqs = np.sort(rng.choice(lay.num_seqs, size=per, replace=False))
+        sub = sample_layout(lay, seqs)
+        dt = oracle_step_seconds(sub, seed=it)
+        if it >= args.warmup:
+            times.append(dt)
+            nbytes.append(kv_bytes(sub.seq_lens, sub.num_kv_heads, sub.head_dim))
+    value = sum(nbytes) / sum(times) / 1e9
+    ms = 1e3 * sum(times) / len(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "decode: 256 seqs x 1 token, history U[512,4096], 32q/32kv, "
+                               "head_dim 128, block_size 16, 70000-block pool",
+                   "sample_per_step": f"{per} random sequences of the 256",
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{per} sequences per step, fp64 numpy"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+def secondary(dev, steps, warmup, peaks):
+    """Prefill and mixed-step measurements (device time only)."""
+    res = {}
+    lay = workloads.config_layout(3, 0)
+    st = Step(lay, dev)
+    ms, attn_ms, _ = time_device(st, steps, warmup, False)
+    fl = attention_flops(lay, np.arange(lay.num_seqs))
+    tf = fl / (attn_ms * 1e-3) / 1e12
+    res["prefill"] = {"workload": "16 prompts (log-uniform 16..2048, sum 8192), 32q/8kv, D 128, bs 16",
+                      "metric": "prefill TFLOP/s", "value": tf, "ms_attention": attn_ms,
+                      "ms_per_step": ms, "flops": fl,
+                      "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16"],
+                                   "unit": "TFLOP/s", "frac": tf / peaks["bf16"]}}
+    del st
+    lay = workloads.config_layout(4, 0)
+    st = Step(lay, dev)
+    ms, attn_ms, _ = time_device(st, steps, warmup, False)
+    dec = np.arange(lay.num_decode_seqs)
+    pre = np.arange(lay.num_decode_seqs, lay.num_seqs)
+    t_star = decode_kernel_bytes(lay, dec) / (peaks["hbm"] * 1e9) + \
+        attention_flops(lay, pre) / (peaks["bf16"] * 1e12)
+    res["mixed"] = {"workload": "240 decodes (history U[128,8192]) + 2 chunks of 3976 on 1024/3000 cached, 32q/8kv",
+                    "metric": "mixed-batch attn tokens/s", "value": lay.num_tokens / (ms * 1e-3),
+                    "ms_per_step": ms, "ms_attention": attn_ms,
+                    "additive_roofline_ms": t_star * 1e3, "frac": t_star * 1e3 / ms}
+    del st
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import paged_kv_cache_133_gb300 as pa
+    pa.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_on = world > 1
+    if dist_on:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    peaks = load_peaks()
+    lay = workloads.config_layout(2, args.seed)
+    step = Step(lay, dev, seed=args.seed + rank)
+    clocks = ClockSampler(local)
+    ms, attn_ms, launches = time_device(step, args.steps, args.warmup, dist_on, clocks)
+    ms = _max_over_ranks(ms, dist_on, dev)
+    attn_ms = _max_over_ranks(attn_ms, dist_on, dev)
+    err = int(step.err.item())
+    if err:
+        raise RuntimeError(f"device error flag {err} during the bench")
+    kvb = kv_bytes(lay.seq_lens, lay.num_kv_heads, lay.head_dim)
+    value = world * kvb / (ms * 1e-3) / 1e9
+    algo = decode_kernel_bytes(lay, np.arange(lay.num_decode_seqs))
+    achieved = algo / (attn_ms * 1e-3) / 1e9
+    digest = source_digest("decode.cu")
+    traffic = measured_traffic("decode_kernel", "decode", digest)
+    e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, dist_on)
+    e2e_ms = _max_over_ranks(e2e_ms, dist_on, dev)
+    sec = None
+    if not args.no_secondary:
+        del step
+        torch.cuda.empty_cache()
+        sec = secondary(dev, args.steps, args.warmup, peaks)
+    if rank != 0:
+        if dist_on:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    cpu = None if args.no_cpu_baseline else cpu_baseline(lay)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode: 256 seqs x 1 token, history U[512,4096], 32q/32kv, "
+                               "head_dim 128, block_size 16, 70000-block pool (seed %d)" % args.seed,
+                   "kv_bytes_per_step": kvb, "l2": "inputs larger than L2 (18 GB pool, 10 GB read per step)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "baseline_metric": BASELINE_METRIC},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (+combine when split)",
+                     "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm"], "traffic": traffic,
+                     "peak_source": peaks["src"], "algorithmic_bytes_per_launch": algo,
+                     "ms_per_launch": attn_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * kvb / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+    }
+    if sec:
+        line["secondary"] = sec
+    print(json.dumps(line), flush=True)
+    if dist_on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,150 @@
+/*
+ * pa.h — C ABI of the paged-KV attention library (one continuous-batching step).
+ *
+ * Terms (all from "vLLM Continuous Batching：从 Forward Shape 理解两个核心参数",
+ * §2.1 and §2.3补充):
+ *   S   number of sequences scheduled this step, T number of new tokens.
+ *   The new tokens of all sequences form one flat [T] batch; sequence s owns
+ *   rows query_start_loc[s] .. query_start_loc[s+1]-1.
+ *   seq_lens[s] = cached history + new tokens of sequence s (its KV length
+ *   after this step).  New token i of sequence s sits at position
+ *   seq_lens[s] - q_s + i, q_s = query_start_loc[s+1] - query_start_loc[s].
+ *   block_tables[s][j] is the physical block holding logical block j of
+ *   sequence s (rows padded with -1), "vLLM 原理" §3.7 item 4.
+ *   slot_mapping[t] = physical_block * block_size + offset is the cache slot
+ *   that flat token t's K/V are written to (§2.3补充 第一步).
+ *
+ * Memory layout (one layer of the "vLLM 原理" §3.6 cache tensor):
+ *   k_cache, v_cache : bf16 [num_blocks, block_size, num_kv_heads, head_dim],
+ *                      contiguous, 16-byte aligned.
+ *   q, out           : bf16 [T, num_q_heads, head_dim]; head_dim contiguous,
+ *                      heads contiguous within a token, token stride given.
+ *   k, v (new)       : bf16 [T, num_kv_heads, head_dim], same convention.
+ *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership: every pointer is a device pointer owned by the caller unless it
+ * says otherwise; the library allocates no device memory and keeps no
+ * pointer after a call returns.  Every call is asynchronous and ordered on
+ * the given stream (a cudaStream_t passed as void*, NULL = default stream);
+ * none synchronises with the host.
+ *
+ * Errors: a problem visible on the host (null pointer, unsupported shape,
+ * workspace too small) returns a non-zero pa_status and launches nothing.  A
+ * problem that only the device can see (bad slot, bad block id, inconsistent
+ * lengths) sets PA_DEV_* bits in *err_flag with atomicOr (err_flag may be
+ * NULL to skip reporting); the offending rows are skipped and their outputs
+ * are unspecified.  No kernel traps and no kernel waits on another block.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent counts     */
+  PA_ERR_UNSUPPORTED = 2, /* head_dim, block_size or head ratio not supported     */
+  PA_ERR_WORKSPACE = 3,   /* workspace smaller than pa_attention_workspace_size()  */
+  PA_ERR_CUDA = 4         /* a launch failed; see pa_last_cuda_error()             */
+} pa_status;
+
+/* Device-side error bits OR-ed into *err_flag. */
+#define PA_DEV_BAD_SLOT 1u   /* slot_mapping entry >= num_blocks * block_size      */
+#define PA_DEV_BAD_BLOCK 2u  /* a live position maps to a block id outside the pool */
+#define PA_DEV_BAD_LEN 4u    /* seq_len < q_len, seq_len > max_blocks*block_size,
+                                q_len > max_query_len or seq_len > max_seq_len     */
+#define PA_DEV_BAD_DECODE 8u /* a row below num_decode_seqs has q_len != 1          */
+#define PA_DEV_BAD_PAIR 16u  /* a copy pair names a block outside the pool          */
+
+/*
+ * pa_write_kv — scatter the new tokens' K and V into the paged cache.
+ * "vLLM Continuous Batching：从 Forward Shape 理解两个核心参数" §2.3补充 第一步;
+ * store_kvcache in "vLLM 原理" §3.7.
+ *
+ *   k, v           bf16 [T, num_kv_heads, head_dim]; row t starts at element
+ *                  t * k_stride_t (resp. v_stride_t).
+ *   k_cache,v_cache bf16 [num_blocks, block_size, num_kv_heads, head_dim].
+ *   slot_mapping   int32 [T]; slot < 0 means "do not write this token".
+ * For every t with slot_mapping[t] = b * block_size + o >= 0:
+ *   k_cache[b, o] = k[t], v_cache[b, o] = v[t]   (bit-exact copy).
+ * Needs num_kv_heads * head_dim % 8 == 0, strides % 8 == 0, 16-byte aligned
+ * pointers.  Slots must be distinct; duplicate slots race.
+ */
+int pa_write_kv(const void* k, const void* v, int64_t k_stride_t, int64_t v_stride_t,
+                void* k_cache, void* v_cache, const int32_t* slot_mapping, int num_tokens,
+                int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                uint32_t* err_flag, void* stream);
+
+/*
+ * pa_attention_workspace_size — bytes of scratch pa_attention needs for the
+ * split-KV decode partials (fp32 running max, sum and weighted value per
+ * split, sequence and query head).  Depends on the current device's SM count;
+ * query it on the device that will run the call.  0 means no workspace.
+ */
+size_t pa_attention_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int max_seq_len);
+
+/*
+ * pa_attention — causal attention of one step's flat query batch over the
+ * paged cache.  Each query attends only to its own sequence's keys at
+ * positions 0 .. its own position ("A 不会看 B", §0 and §2.3 of the first
+ * page); keys are read through block_tables (§2.3补充 第二步); the new
+ * tokens' K/V must already be in the cache (call pa_write_kv first on the same
+ * stream, as "vLLM 原理" §3.7 Attention.forward does).
+ *
+ *   out      bf16 [T, num_q_heads, head_dim], token stride out_stride_t.
+ *   q        bf16 [T, num_q_heads, head_dim], token stride q_stride_t.
+ *   query_start_loc int32 [S+1], seq_lens int32 [S],
+ *   block_tables    int32 [S, max_blocks_per_seq], -1 padded.
+ *   num_decode_seqs sequences [0, num_decode_seqs) must have exactly one new
+ *                   token; they run on the split-KV decode kernel, the rest
+ *                   on the prefill kernel.  0 is always correct.
+ *   max_query_len, max_seq_len  host-known upper bounds of q_s and seq_lens[s]
+ *                   (like max_seqlen_q / max_seqlen_k of "vLLM 原理" §3.7).
+ *   scale    softmax scale (1/sqrt(head_dim) in the usual case).
+ *   workspace, workspace_bytes  device scratch of at least
+ *                   pa_attention_workspace_size(num_decode_seqs, ...) bytes.
+ * out[t, h] = sum_p softmax_p(scale * q[t,h] . k_p) v_p over the visible keys
+ * of t's sequence, accumulated in fp32, rounded once to bf16.
+ * Supports head_dim 64 or 128, block_size a power of two in [1, 256],
+ * num_q_heads % num_kv_heads == 0.  Rows of sequences with q_s = 0 are untouched.
+ */
+int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                 const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
+                 const int32_t* seq_lens, const int32_t* block_tables, int num_seqs,
+                 int num_tokens, int max_blocks_per_seq, int num_decode_seqs, int max_query_len,
+                 int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                 int block_size, int num_blocks, float scale, void* workspace,
+                 size_t workspace_bytes, uint32_t* err_flag, void* stream);
+
+/*
+ * pa_copy_blocks — copy-on-write block copies, "vLLM 原理" §2.1: for each
+ * pair (src, dst) in pairs (int32 [num_pairs, 2], device memory),
+ * k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src], all
+ * block_size slots, bit-exact.  Destinations must be distinct and must not be
+ * the source of any pair (copy-on-write always copies into a fresh block);
+ * otherwise the result is unspecified.
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                   int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                   uint32_t* err_flag, void* stream);
+
+/* Human-readable name of a pa_status value (static string). */
+const char* pa_status_string(int status);
+
+/* The cudaError_t of the last call that returned PA_ERR_CUDA on this thread. */
+int pa_last_cuda_error(void);
+
+/* Number of kernels this library has launched since it was loaded (all threads). */
+uint64_t pa_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

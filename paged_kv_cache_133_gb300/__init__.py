@@ -1,0 +1,201 @@
+"""Python binding of the paged-KV attention C ABI (``include/pa.h``).
+
+Argument marshalling only: torch tensors become raw device pointers, strides
+and sizes, and the current CUDA stream is passed through.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback.  If the
+library has not been built the first call raises.
+
+    write_kv(k, v, k_cache, v_cache, slot_mapping)
+    attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, ...)
+    copy_blocks(k_cache, v_cache, pairs)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = ["write_kv", "attention", "copy_blocks", "workspace_size", "kernel_launches",
+           "library_path", "load", "PaError", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN",
+           "DEV_BAD_DECODE", "DEV_BAD_PAIR"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_lib", "libpa133.so")
+_lib = None
+
+DEV_BAD_SLOT = 1
+DEV_BAD_BLOCK = 2
+DEV_BAD_LEN = 4
+DEV_BAD_DECODE = 8
+DEV_BAD_PAIR = 16
+
+_c_i = ctypes.c_int
+_c_i64 = ctypes.c_int64
+_c_p = ctypes.c_void_p
+_c_sz = ctypes.c_size_t
+_c_f = ctypes.c_float
+
+_SIGNATURES = {
+    "pa_write_kv": (_c_i, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i,
+                           _c_i, _c_p, _c_p]),
+    "pa_attention_workspace_size": (_c_sz, [_c_i, _c_i, _c_i, _c_i, _c_i]),
+    "pa_attention": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i,
+                            _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_f, _c_p,
+                            _c_sz, _c_p, _c_p]),
+    "pa_copy_blocks": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_p, _c_p]),
+    "pa_status_string": (ctypes.c_char_p, [_c_i]),
+    "pa_last_cuda_error": (_c_i, []),
+    "pa_kernel_launches": (ctypes.c_uint64, []),
+}
+
+
+class PaError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load ``libpa133.so`` (raises if it is missing: build it first)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise PaError(f"CUDA library not built: {_LIB_PATH} is missing "
+                      "(run `python -m paged_kv_cache_133_gb300.build`)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        lib = load()
+        msg = lib.pa_status_string(rc).decode()
+        if msg == "PA_ERR_CUDA":
+            msg += f" (cudaError {lib.pa_last_cuda_error()})"
+        raise PaError(f"{what}: {msg}")
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _bf16_rows(t, name):
+    import torch
+    _need(t.dtype == torch.bfloat16, f"{name} must be bfloat16")
+    _need(t.is_cuda, f"{name} must be on a CUDA device")
+    _need(t.dim() == 3, f"{name} must be [tokens, heads, head_dim]")
+    _need(t.stride(2) == 1 and t.stride(1) == t.shape[2], f"{name}: heads x head_dim must be contiguous")
+
+
+def _i32(t, name):
+    import torch
+    _need(t.dtype == torch.int32 and t.is_cuda and t.is_contiguous(),
+          f"{name} must be a contiguous int32 CUDA tensor")
+
+
+def _cache(t, name):
+    import torch
+    _need(t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous() and t.dim() == 4,
+          f"{name} must be a contiguous bf16 CUDA tensor [num_blocks, block_size, kv_heads, head_dim]")
+
+
+def kernel_launches() -> int:
+    return int(load().pa_kernel_launches())
+
+
+def write_kv(k, v, k_cache, v_cache, slot_mapping, err=None, stream=None):
+    """Scatter new-token K/V rows into the paged cache through ``slot_mapping``."""
+    _bf16_rows(k, "k")
+    _bf16_rows(v, "v")
+    _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    _i32(slot_mapping, "slot_mapping")
+    nb, bs, hkv, d = k_cache.shape
+    _need(tuple(v_cache.shape) == (nb, bs, hkv, d), "k_cache and v_cache shapes differ")
+    _need(k.shape[1:] == (hkv, d) and v.shape[1:] == (hkv, d), "k/v head shape mismatch")
+    T = slot_mapping.numel()
+    _need(k.shape[0] >= T and v.shape[0] >= T, "k/v have fewer rows than slot_mapping")
+    rc = load().pa_write_kv(_ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(k_cache), _ptr(v_cache),
+                            _ptr(slot_mapping), T, nb, bs, hkv, d, _ptr(err), _stream(stream))
+    _check(rc, "pa_write_kv")
+
+
+def copy_blocks(k_cache, v_cache, pairs, err=None, stream=None):
+    """Copy-on-write: ``cache[dst] = cache[src]`` for each row (src, dst) of ``pairs``."""
+    _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    _i32(pairs, "pairs")
+    nb, bs, hkv, d = k_cache.shape
+    n = pairs.numel() // 2
+    rc = load().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), n, nb, bs, hkv, d,
+                               _ptr(err), _stream(stream))
+    _check(rc, "pa_copy_blocks")
+
+
+def workspace_size(num_decode_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len) -> int:
+    """Bytes of scratch ``attention`` needs on the current device."""
+    return int(load().pa_attention_workspace_size(num_decode_seqs, num_q_heads, num_kv_heads,
+                                                  head_dim, max_seq_len))
+
+
+def attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, *, num_decode_seqs,
+              max_query_len, max_seq_len, scale=None, out=None, workspace=None, err=None,
+              stream=None):
+    """Causal paged attention of one step's flat query batch; returns ``out`` [T, Hq, D] bf16.
+
+    ``max_query_len`` / ``max_seq_len`` are host-side upper bounds (no device
+    sync happens here).  ``workspace`` is allocated with torch when not given
+    and the call needs one.
+    """
+    import torch
+    _bf16_rows(q, "q")
+    _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
+                 (block_tables, "block_tables")):
+        _i32(t, n)
+    _need(block_tables.dim() == 2, "block_tables must be [num_seqs, max_blocks_per_seq]")
+    nb, bs, hkv, d = k_cache.shape
+    T, hq, dq = q.shape
+    _need(dq == d, "q head_dim differs from the cache's")
+    S = seq_lens.numel()
+    _need(query_start_loc.numel() == S + 1 and block_tables.shape[0] == S, "metadata sizes differ")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _bf16_rows(out, "out")
+        _need(out.shape == q.shape, "out shape differs from q")
+    need = workspace_size(num_decode_seqs, hq, hkv, d, max_seq_len)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().pa_attention(_ptr(out), out.stride(0), _ptr(q), q.stride(0), _ptr(k_cache),
+                             _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens),
+                             _ptr(block_tables), S, T, block_tables.shape[1], num_decode_seqs,
+                             max_query_len, max_seq_len, hq, hkv, d, bs, nb, float(scale),
+                             _ptr(workspace), wbytes, _ptr(err), _stream(stream))
+    _check(rc, "pa_attention")
+    return out

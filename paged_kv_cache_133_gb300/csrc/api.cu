@@ -1,0 +1,196 @@
+// C ABI entry points: host-side validation, workspace sizing and dispatch.
+// Nothing here allocates device memory or synchronises with the device.
+#include <math.h>
+
+#include <atomic>
+
+#include "internal.h"
+#include "pa.h"
+
+namespace pa {
+
+static std::atomic<uint64_t> g_launches{0};
+static thread_local int g_last_cuda_error = 0;
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static int num_sms_of_current_device() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PA_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  return PA_ERR_CUDA;
+}
+
+static int ilog2_exact(int x) {
+  if (x <= 0 || (x & (x - 1))) return -1;
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+static size_t decode_workspace(int num_decode, int hq, int hkv, int head_dim, int max_seq_len,
+                               int* part, int* nsplit) {
+  *part = 64;
+  *nsplit = 1;
+  if (num_decode <= 0 || hkv <= 0 || hq <= 0 || hq % hkv || max_seq_len <= 0) return 0;
+  const int group = hq / hkv;
+  const int units = hkv * ((group + 15) / 16);
+  decode_partition(num_decode, units, max_seq_len, num_sms_of_current_device(), part, nsplit);
+  if (*nsplit <= 1) return 0;
+  return static_cast<size_t>(*nsplit) * num_decode * hq * (head_dim + 2) * sizeof(float);
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    default: return "PA_ERR_UNKNOWN";
+  }
+}
+
+int pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t pa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int pa_write_kv(const void* k, const void* v, int64_t k_stride_t, int64_t v_stride_t,
+                void* k_cache, void* v_cache, const int32_t* slot_mapping, int num_tokens,
+                int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                uint32_t* err_flag, void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!k || !v || !slot_mapping)) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row % 8 || k_stride_t % 8 || v_stride_t % 8 || k_stride_t < row || v_stride_t < row)
+    return PA_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || (num_tokens > 0 && (!aligned16(k) || !aligned16(v))))
+    return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  return cuda_status(launch_write_kv(k, v, k_stride_t, v_stride_t, k_cache, v_cache, slot_mapping,
+                                     num_tokens, num_blocks, block_size, static_cast<int>(row),
+                                     err_flag, static_cast<cudaStream_t>(stream)));
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                   int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                   uint32_t* err_flag, void* stream) {
+  if (num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache || (num_pairs > 0 && !pairs)) return PA_ERR_INVALID_ARG;
+  if (num_pairs > 65535) return PA_ERR_UNSUPPORTED;
+  const int64_t elems = static_cast<int64_t>(block_size) * num_kv_heads * head_dim;
+  if (elems % 8 || elems > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  return cuda_status(launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks,
+                                        static_cast<int>(elems), err_flag,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_attention_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int max_seq_len) {
+  int part, nsplit;
+  return decode_workspace(num_decode_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                          &part, &nsplit);
+}
+
+int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                 const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
+                 const int32_t* seq_lens, const int32_t* block_tables, int num_seqs,
+                 int num_tokens, int max_blocks_per_seq, int num_decode_seqs, int max_query_len,
+                 int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                 int block_size, int num_blocks, float scale, void* workspace,
+                 size_t workspace_bytes, uint32_t* err_flag, void* stream) {
+  if (num_seqs < 0 || num_tokens < 0 || num_decode_seqs < 0 || num_decode_seqs > num_seqs ||
+      max_query_len < 0 || max_seq_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  const int bs_log2 = ilog2_exact(block_size);
+  if (bs_log2 < 0 || block_size > 256) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !query_start_loc || !seq_lens || !block_tables)
+    return PA_ERR_INVALID_ARG;
+  if (q_stride_t % 8 || out_stride_t % 8 ||
+      q_stride_t < static_cast<int64_t>(num_q_heads) * head_dim ||
+      out_stride_t < static_cast<int64_t>(num_q_heads) * head_dim)
+    return PA_ERR_UNSUPPORTED;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_UNSUPPORTED;
+  const int group = num_q_heads / num_kv_heads;
+  const int64_t hunits = static_cast<int64_t>(num_kv_heads) * ((group + 15) / 16);
+  if (num_decode_seqs > 65535 || num_seqs - num_decode_seqs > 65535 || hunits > 65535)
+    return PA_ERR_UNSUPPORTED;
+
+  AttnArgs a{};
+  a.out = out;
+  a.out_stride = out_stride_t;
+  a.q = q;
+  a.q_stride = q_stride_t;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.qsl = query_start_loc;
+  a.seq_lens = seq_lens;
+  a.block_tables = block_tables;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_decode = num_decode_seqs;
+  a.max_query_len = max_query_len;
+  a.max_seq_len = max_seq_len;
+  a.hq = num_q_heads;
+  a.hkv = num_kv_heads;
+  a.group = group;
+  a.head_dim = head_dim;
+  a.bs_log2 = bs_log2;
+  a.num_blocks = num_blocks;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = err_flag;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (num_decode_seqs > 0 && max_seq_len > 0) {
+    const size_t need = decode_workspace(num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
+                                         max_seq_len, &a.part, &a.nsplit);
+    if (need > 0) {
+      if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return PA_ERR_WORKSPACE;
+      a.ws_o = static_cast<float*>(workspace);
+      a.ws_ml = a.ws_o + static_cast<size_t>(a.nsplit) * num_decode_seqs * num_q_heads * head_dim;
+    }
+    int rc = cuda_status(launch_decode(a, st));
+    if (rc != PA_OK) return rc;
+  }
+  if (num_seqs > num_decode_seqs && max_query_len > 0) {
+    int rc = cuda_status(launch_prefill(a, st));
+    if (rc != PA_OK) return rc;
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// Host-side launch interface between the C ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+void count_launch();
+
+struct AttnArgs {
+  void* out;
+  int64_t out_stride;  // elements between tokens
+  const void* q;
+  int64_t q_stride;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* block_tables;
+  int num_seqs;
+  int num_tokens;
+  int max_blocks;
+  int num_decode;
+  int max_query_len;
+  int max_seq_len;
+  int hq, hkv, group;  // group = hq / hkv
+  int head_dim;
+  int bs_log2;
+  int num_blocks;
+  float scale_log2;  // scale * log2(e)
+  uint32_t* err;
+  // split-KV decode
+  int part;      // tokens per split
+  int nsplit;    // grid splits = ceil(max_seq_len / part)
+  float* ws_o;   // [nsplit, num_decode, hq, head_dim]
+  float* ws_ml;  // [nsplit, num_decode, hq, 2]
+};
+
+// Split-KV partition for the decode rows; shared by the workspace query and the
+// launch so that both agree.
+void decode_partition(int num_decode, int hkv_units, int max_seq_len, int num_sms, int* part,
+                      int* nsplit);
+
+cudaError_t launch_write_kv(const void* k, const void* v, int64_t ks, int64_t vs, void* kc,
+                            void* vc, const int32_t* slots, int T, int num_blocks, int bs,
+                            int row_elems, uint32_t* err, cudaStream_t st);
+cudaError_t launch_copy_blocks(void* kc, void* vc, const int32_t* pairs, int n, int num_blocks,
+                               int block_elems, uint32_t* err, cudaStream_t st);
+cudaError_t launch_decode(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t st);
+
+}  // namespace pa

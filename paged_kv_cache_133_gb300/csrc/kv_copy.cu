@@ -1,0 +1,93 @@
+// KV-cache scatter through slot_mapping and copy-on-write block copies.
+//
+// Both are pure data movement: 16-byte vector loads and stores, consecutive
+// threads on consecutive 16-byte pieces of one token row (or one block), so
+// every warp moves 512 contiguous bytes per instruction.
+#include "common.cuh"
+#include "internal.h"
+
+namespace pa {
+
+// One thread per 16-byte piece of a [num_kv_heads * head_dim] token row.
+// "vLLM Continuous Batching：从 Forward Shape 理解两个核心参数" §2.3补充 第一步:
+// token t's K/V go to slot_mapping[t] = block * block_size + offset, which is
+// row `slot` of the cache viewed as [num_blocks * block_size, kv_heads, dim].
+__global__ void __launch_bounds__(256) write_kv_kernel(const uint4* __restrict__ k,
+                                                       const uint4* __restrict__ v, int64_t ks,
+                                                       int64_t vs, uint4* __restrict__ kc,
+                                                       uint4* __restrict__ vc,
+                                                       const int32_t* __restrict__ slots, int T,
+                                                       int vec_per_row, int64_t num_slots,
+                                                       uint32_t* err) {
+  const int64_t total = static_cast<int64_t>(T) * vec_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / vec_per_row);
+    const int c = static_cast<int>(i - static_cast<int64_t>(t) * vec_per_row);
+    const int slot = __ldg(slots + t);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (c == 0) flag_error(err, PA_DEV_BAD_SLOT);
+      continue;
+    }
+    const uint4 kv = __ldg(k + t * ks + c);
+    const uint4 vv = __ldg(v + t * vs + c);
+    const int64_t o = static_cast<int64_t>(slot) * vec_per_row + c;
+    kc[o] = kv;
+    vc[o] = vv;
+  }
+}
+
+// blockIdx.y = pair; threads stride over the block's 16-byte pieces.
+// "vLLM 原理" §2.1: the fresh block receives the shared block's whole contents.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ kc,
+                                                          uint4* __restrict__ vc,
+                                                          const int32_t* __restrict__ pairs,
+                                                          int num_blocks, int vec_per_block,
+                                                          uint32_t* err) {
+  const int p = blockIdx.y;
+  const int src = __ldg(pairs + 2 * p), dst = __ldg(pairs + 2 * p + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, PA_DEV_BAD_PAIR);
+    return;
+  }
+  const int64_t so = static_cast<int64_t>(src) * vec_per_block;
+  const int64_t d = static_cast<int64_t>(dst) * vec_per_block;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < vec_per_block;
+       i += gridDim.x * blockDim.x) {
+    const uint4 a = kc[so + i];
+    const uint4 b = vc[so + i];
+    kc[d + i] = a;
+    vc[d + i] = b;
+  }
+}
+
+cudaError_t launch_write_kv(const void* k, const void* v, int64_t ks, int64_t vs, void* kc,
+                            void* vc, const int32_t* slots, int T, int num_blocks, int bs,
+                            int row_elems, uint32_t* err, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int vpr = row_elems / 8;
+  const int64_t total = static_cast<int64_t>(T) * vpr;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  count_launch();
+  write_kv_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), ks / 8, vs / 8,
+      static_cast<uint4*>(kc), static_cast<uint4*>(vc), slots, T, vpr,
+      static_cast<int64_t>(num_blocks) * bs, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* kc, void* vc, const int32_t* pairs, int n, int num_blocks,
+                               int block_elems, uint32_t* err, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int vpb = block_elems / 8;
+  int bx = (vpb + 255) / 256;
+  if (bx > 8) bx = 8;
+  count_launch();
+  copy_blocks_kernel<<<dim3(bx, n), 256, 0, st>>>(static_cast<uint4*>(kc), static_cast<uint4*>(vc),
+                                                   pairs, num_blocks, vpb, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pa
