@@ -406,6 +406,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-seqs", type=int, default=0,
+                    help="profile case: only the first N decode sequences, pool sized to fit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -430,6 +432,9 @@ def main():
 
     peaks = load_peaks()
     lay = workloads.config_layout(2, args.seed)
+    if args.decode_seqs:
+        lay = sample_layout(lay, np.arange(min(args.decode_seqs, lay.num_seqs)))
+        lay.num_blocks = int(lay.num_blocks * 1.1) + 1
     step = Step(lay, dev, seed=args.seed + rank)
     clocks = ClockSampler(local)
     ms, attn_ms, launches = time_device(step, args.steps, args.warmup, dist_on, clocks)

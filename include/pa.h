@@ -134,6 +134,38 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
                    int num_blocks, int block_size, int num_kv_heads, int head_dim,
                    uint32_t* err_flag, void* stream);
 
+/*
+ * pa_attention_noalloc — pa_attention without a workspace argument, for
+ * callers that cannot allocate device memory (a library embedded in a host
+ * application that owns every device allocation, a runtime whose memory is
+ * reserved up front, or a loop that must not call cudaMalloc, which can wait
+ * for the whole device).  The pages have no counterpart: this is a calling
+ * convention of this library, not part of the method.
+ *
+ * Same arguments, result and errors as pa_attention minus workspace and
+ * workspace_bytes.  The split-KV scratch is a static device array of
+ * PA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.  A call whose decode
+ * rows would need more scratch than that returns PA_ERR_WORKSPACE and
+ * launches nothing (use pa_attention with a workspace instead).
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.  A
+ * failed lookup returns PA_ERR_CUDA without updating pa_last_cuda_error.
+ * Every call shares the array and it keeps the previous call's contents;
+ * nothing in it has to start at zero.  Calls that overlap on the GPU (other
+ * streams or host threads) race on the array: serialise them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int pa_attention_noalloc(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                         const void* k_cache, const void* v_cache,
+                         const int32_t* query_start_loc, const int32_t* seq_lens,
+                         const int32_t* block_tables, int num_seqs, int num_tokens,
+                         int max_blocks_per_seq, int num_decode_seqs, int max_query_len,
+                         int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int num_blocks, float scale, uint32_t* err_flag,
+                         void* stream);
+
 /* Human-readable name of a pa_status value (static string). */
 const char* pa_status_string(int status);
 

@@ -16,7 +16,7 @@ import ctypes
 import math
 import os
 
-__all__ = ["write_kv", "attention", "copy_blocks", "workspace_size", "kernel_launches",
+__all__ = ["write_kv", "attention", "attention_noalloc", "copy_blocks", "workspace_size", "kernel_launches",
            "library_path", "load", "PaError", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN",
            "DEV_BAD_DECODE", "DEV_BAD_PAIR"]
 
@@ -44,6 +44,9 @@ _SIGNATURES = {
                             _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_f, _c_p,
                             _c_sz, _c_p, _c_p]),
     "pa_copy_blocks": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_p, _c_p]),
+    "pa_attention_noalloc": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i,
+                                    _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
+                                    _c_f, _c_p, _c_p]),
     "pa_status_string": (ctypes.c_char_p, [_c_i]),
     "pa_last_cuda_error": (_c_i, []),
     "pa_kernel_launches": (ctypes.c_uint64, []),
@@ -198,4 +201,41 @@ def attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, *, n
                              max_query_len, max_seq_len, hq, hkv, d, bs, nb, float(scale),
                              _ptr(workspace), wbytes, _ptr(err), _stream(stream))
     _check(rc, "pa_attention")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def attention_noalloc(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, *, out,
+                      num_decode_seqs, max_query_len, max_seq_len, scale=None, err=None,
+                      stream=None):
+    """``attention`` for callers that cannot allocate device memory.
+
+    Takes a caller-provided ``out`` and no workspace: the split-KV scratch is a
+    static device array of ``NOALLOC_SCRATCH_BYTES`` inside the library, shared
+    by every call (calls that overlap on the GPU race on it).  Nothing here
+    allocates.  Raises ``PaError`` (PA_ERR_WORKSPACE) when the batch's decode
+    rows need more scratch than the array holds.
+    """
+    _bf16_rows(q, "q")
+    _bf16_rows(out, "out")
+    _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
+                 (block_tables, "block_tables")):
+        _i32(t, n)
+    nb, bs, hkv, d = k_cache.shape
+    T, hq, _ = q.shape
+    _need(out.shape == q.shape, "out shape differs from q")
+    S = seq_lens.numel()
+    _need(query_start_loc.numel() == S + 1 and block_tables.shape[0] == S, "metadata sizes differ")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = load().pa_attention_noalloc(_ptr(out), out.stride(0), _ptr(q), q.stride(0), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens),
+                                     _ptr(block_tables), S, T, block_tables.shape[1],
+                                     num_decode_seqs, max_query_len, max_seq_len, hq, hkv, d, bs,
+                                     nb, float(scale), _ptr(err), _stream(stream))
+    _check(rc, "pa_attention_noalloc")
     return out
