@@ -60,6 +60,8 @@ typedef enum {
                                 q_len > max_query_len or seq_len > max_seq_len     */
 #define PA_DEV_BAD_DECODE 8u /* a row below num_decode_seqs has q_len != 1          */
 #define PA_DEV_BAD_PAIR 16u  /* a copy pair names a block outside the pool          */
+#define PA_DEV_TIMEOUT 32u   /* a pipeline wait inside a kernel ran out of time (2 s);
+                                the kernel drained and exited, outputs unspecified   */
 
 /*
  * pa_write_kv — scatter the new tokens' K and V into the paged cache.

@@ -51,4 +51,10 @@ cudaError_t launch_copy_blocks(void* kc, void* vc, const int32_t* pairs, int n, 
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t st);
 
+// Tensor-core (tcgen05) prefill: whether the shapes and the environment allow
+// it, and its launch (cudaErrorNotSupported, with nothing launched, when a
+// TMA descriptor cannot be encoded).
+bool prefill_tc_supported(const AttnArgs& a);
+cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t st);
+
 }  // namespace pa

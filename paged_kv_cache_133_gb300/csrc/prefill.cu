@@ -1,6 +1,8 @@
 // Ragged causal attention for rows with any number of new tokens (prefill and
 // chunked prefill), on mma.sync tensor-core tiles.  This is the general path:
-// any head_dim in {64, 128}, any power-of-two block size, any GQA ratio.
+// any head_dim in {64, 128}, any power-of-two block size, any GQA ratio.  The
+// tcgen05 kernel (prefill_tc.cu) takes over whenever it supports the shapes
+// (block size >= 8); PA_PREFILL_IMPL=mma forces this one.
 //
 // Work unit: one CTA per (64-row query tile, kv head, sequence).  The rows of
 // a sequence's tile are (new token i, query head of the kv head's group)
@@ -269,6 +271,10 @@ cudaError_t launch_prefill_d(const AttnArgs& a, cudaStream_t st) {
 
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t st) {
   if (a.num_seqs - a.num_decode <= 0 || a.max_query_len <= 0) return cudaSuccess;
+  if (prefill_tc_supported(a)) {
+    const cudaError_t e = launch_prefill_tc(a, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
   return a.head_dim == 128 ? launch_prefill_d<128>(a, st) : launch_prefill_d<64>(a, st);
 }
 

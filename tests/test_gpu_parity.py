@@ -228,3 +228,54 @@ def test_empty_batch_is_a_no_op():
     pa.write_kv(g["k"][:0], g["v"][:0], g["k_cache"], g["v_cache"], z)
     assert pa.kernel_launches() == before
     assert torch.equal(k0, g["k_cache"])
+
+
+@pytest.fixture(params=["tc", "mma"])
+def prefill_impl(request, monkeypatch):
+    """Run a test once on the tcgen05 prefill kernel and once on the mma.sync one."""
+    if request.param == "mma":
+        monkeypatch.setenv("PA_PREFILL_IMPL", "mma")
+    else:
+        monkeypatch.delenv("PA_PREFILL_IMPL", raising=False)
+    return request.param
+
+
+def _prefill_cases():
+    rng = np.random.default_rng(23)
+    out = []
+    for i, (hq, hkv, d, bs) in enumerate([(8, 2, 128, 16), (4, 4, 64, 16), (8, 1, 128, 8),
+                                           (4, 2, 128, 256), (12, 4, 64, 32), (2, 2, 128, 128)]):
+        cached = [0, int(rng.integers(1, 400)), 0, int(rng.integers(100, 900))]
+        queries = [int(rng.integers(1, 300)), int(rng.integers(100, 260)), 128, int(rng.integers(2, 40))]
+        nb = sum(-(-(c + q) // bs) for c, q in zip(cached, queries)) + 5
+        out.append(workloads.custom_layout(f"pf{i}_h{hq}x{hkv}_d{d}_bs{bs}", cached, queries, hq, hkv,
+                                           d, bs, nb, 200 + i))
+    return out
+
+
+@pytest.mark.parametrize("lay", _prefill_cases(), ids=lambda l: l.name)
+def test_prefill_kernels_match_oracle(lay, prefill_impl):
+    ts = workloads.make_tensors(lay, seed=8, poison=True)
+    g = {k: v.to(DEV) for k, v in ts.items()}
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = H.run_step(lay, g, H.device_meta(lay, DEV), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    H.assert_close(H.f64(out), H.oracle_full(lay, ts), f"{lay.name}/{prefill_impl}")
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+def test_prefill_full_size_both_kernels_agree(cfg, monkeypatch):
+    # the tensor-core and the general kernel on the same full-size batch
+    lay = workloads.config_layout(cfg, 0)
+    g = workloads.make_tensors(lay, seed=0, device=DEV)
+    md = H.device_meta(lay, DEV)
+    monkeypatch.delenv("PA_PREFILL_IMPL", raising=False)
+    out_tc = H.run_step(lay, g, md).clone()
+    monkeypatch.setenv("PA_PREFILL_IMPL", "mma")
+    out_mma = H.run_step(lay, g, md).clone()
+    torch.cuda.synchronize()
+    rows = slice(lay.num_decode_seqs, None)
+    d = (out_tc.float() - out_mma.float()).abs()
+    assert torch.isfinite(out_tc.float()).all()
+    assert d.max().item() <= 2e-2 and d.mean().item() <= 2e-3
