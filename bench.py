@@ -397,6 +397,54 @@ def secondary(dev, steps, warmup, peaks):
     return res
 
 
+def run_other(args, dev, peaks, rank, world, dist_on):
+    """One JSON line for the prefill, mixed or shared-prefix workload."""
+    cfg = {"prefill": 3, "mixed": 4, "shared": 5}[args.workload]
+    lay = workloads.config_layout(cfg, args.seed)
+    step = Step(lay, dev, seed=args.seed + rank)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    ms, attn_ms, launches = time_device(step, args.steps, args.warmup, dist_on, clocks)
+    ms = _max_over_ranks(ms, dist_on, dev)
+    attn_ms = _max_over_ranks(attn_ms, dist_on, dev)
+    e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, dist_on)
+    e2e_ms = _max_over_ranks(e2e_ms, dist_on, dev)
+    if rank != 0:
+        return
+    dec = np.arange(lay.num_decode_seqs)
+    pre = np.arange(lay.num_decode_seqs, lay.num_seqs)
+    if args.workload == "prefill":
+        fl = attention_flops(lay, pre)
+        value, unit, metric = world * fl / (ms * 1e-3) / 1e12, "TFLOP/s", "prefill TFLOP/s"
+        ach = fl / (attn_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16"]}
+        e2e_v = world * fl / (e2e_ms * 1e-3) / 1e12
+    elif args.workload == "mixed":
+        value, unit, metric = world * lay.num_tokens / (ms * 1e-3), "tokens/s", "mixed-batch attn tokens/s"
+        t_star = decode_kernel_bytes(lay, dec) / (peaks["hbm"] * 1e9) + \
+            attention_flops(lay, pre) / (peaks["bf16"] * 1e12)
+        roof = {"bound": "hbm+tensor (additive)", "achieved_ms": attn_ms, "ideal_ms": t_star * 1e3,
+                "frac": t_star * 1e3 / attn_ms}
+        e2e_v = world * lay.num_tokens / (e2e_ms * 1e-3)
+    else:
+        kvb = kv_bytes(lay.seq_lens, lay.num_kv_heads, lay.head_dim)
+        value, unit, metric = world * kvb / (ms * 1e-3) / 1e9, "GB/s", "logical KV-read GB/s"
+        ach = decode_kernel_bytes(lay, dec) / (attn_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm (logical bytes; the shared prefix is L2-resident)", "achieved": ach,
+                "peak": peaks["hbm"], "unit": "GB/s", "frac": ach / peaks["hbm"]}
+        e2e_v = world * kvb / (e2e_ms * 1e-3) / 1e9
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": lay.name, "ms_attention": attn_ms,
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roof, "cpu_baseline": None,
+            "e2e": {"value": e2e_v, "unit": unit, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -406,6 +454,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["decode", "prefill", "mixed", "shared"], default="decode",
+                    help="decode is the headline; the others print their own metric")
     ap.add_argument("--decode-seqs", type=int, default=0,
                     help="profile case: only the first N decode sequences, pool sized to fit")
     args = ap.parse_args()
@@ -431,6 +481,9 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     peaks = load_peaks()
+    if args.workload != "decode":
+        run_other(args, dev, peaks, rank, world, dist_on)
+        return
     lay = workloads.config_layout(2, args.seed)
     if args.decode_seqs:
         lay = sample_layout(lay, np.arange(min(args.decode_seqs, lay.num_seqs)))
