@@ -14,7 +14,7 @@ static thread_local int g_last_cuda_error = 0;
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-static int num_sms_of_current_device() {
+int device_num_sms() {
   static int cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -48,7 +48,7 @@ static size_t decode_workspace(int num_decode, int hq, int hkv, int head_dim, in
   if (num_decode <= 0 || hkv <= 0 || hq <= 0 || hq % hkv || max_seq_len <= 0) return 0;
   const int group = hq / hkv;
   const int units = hkv * ((group + 15) / 16);
-  decode_partition(num_decode, units, max_seq_len, num_sms_of_current_device(), part, nsplit);
+  decode_partition(num_decode, units, max_seq_len, device_num_sms(), part, nsplit);
   if (*nsplit <= 1) return 0;
   return static_cast<size_t>(*nsplit) * num_decode * hq * (head_dim + 2) * sizeof(float);
 }

@@ -9,6 +9,9 @@ namespace pa {
 
 void count_launch();
 
+// SM count of the current device (cached per device).
+int device_num_sms();
+
 struct AttnArgs {
   void* out;
   int64_t out_stride;  // elements between tokens

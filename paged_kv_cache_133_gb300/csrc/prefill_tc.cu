@@ -1,33 +1,44 @@
 // Ragged causal prefill on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// Work unit: one CTA per (128-query tile, query head, sequence).  Query token
-// i of a sequence with c cached tokens sits at position c + i and sees keys
-// 0 .. c + i of its own sequence (bottom-right aligned causal mask; "vLLM 原理"
-// §3.7: new queries attend to the whole cached sequence).  Keys are consumed
-// in tiles of 128 positions; each tile is gathered from the paged cache by TMA,
-// one box per physical block found through the sequence's block table ("vLLM
-// Continuous Batching：从 Forward Shape 理解两个核心参数" §2.3补充 第二步).
+// Query token i of a sequence with c cached tokens sits at position c + i and
+// sees keys 0 .. c + i of its own sequence (bottom-right aligned causal mask;
+// "vLLM 原理" §3.7: new queries attend to the whole cached sequence).  Keys
+// are consumed in tiles of 128 positions; each tile is gathered from the
+// paged cache by TMA, one box per physical block found through the sequence's
+// block table ("vLLM Continuous Batching：从 Forward Shape 理解两个核心参数"
+// §2.3补充 第二步).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax + epilogue; thread r owns query row r = TMEM lane r
-//   warp 4     TMA producer: Q once, then K_j / V_j into a 2-stage ring
-//   warp 5     TMEM allocation and MMA issue (one elected lane)
-// Per key tile j:
-//   S_j = Q K_j^T        tcgen05.mma kind::f16, 128x128x(head_dim), fp32 in TMEM
-//                        (two S buffers, so S_{j+1} runs while row j's softmax does)
-//   softmax              tcgen05.ld of the row, mask, scale, online max / sum,
-//                        P = 2^(s - m) rounded to bf16 into 128B-swizzled smem
-//   O += P V_j           tcgen05.mma with V read MN-major; O stays in TMEM
-// The running max m only moves when a row's tile maximum exceeds it by more
-// than 8 (a factor 256 in the exponent base 2); O and l are then rescaled by
-// 2^(m_old - m_new).  Because numerator and denominator use the same m the
-// result is exact for any choice of m; the threshold only bounds P <= 256.
-// All scores are in the log2 domain (scale pre-multiplied by log2 e).
+// Work item: 128 query tokens of one sequence for TWO query heads A and B of
+// the same kv head (so every K/V tile feeds both), or one head when the group
+// has an odd head left over.  The grid is persistent (one CTA per SM); CTAs
+// walk the item list in a boustrophedon order over "tile counted from the
+// end of its sequence", so the longest key ranges start first.
 //
-// Every mbarrier wait is bounded (2 s of wall time); on expiry the kernel sets
-// PA_DEV_TIMEOUT, lets its in-flight copies and MMAs drain (again bounded),
-// frees TMEM and exits.
+// Warp roles (320 threads):
+//   warps 0-3  softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
+//   warps 4-7  softmax + epilogue of tile B
+//   warp 8     TMA producer: Q_A/Q_B per item, K_j and V_j into 2-stage rings
+//   warp 9     TMEM allocation and MMA issue (one lane)
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// Per key tile j the tensor core runs, in issue order,
+//   PV_A(j-1) .. S_A(j) .. PV_B(j-1) .. S_B(j) ..
+// so while softmax A works on S_A(j) the tensor core computes B's products and
+// the other way round (the two tiles ping-pong).  S = Q K^T and O += P V are
+// tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) with operands in 128-byte-
+// swizzled shared memory; V is read MN-major.  P (bf16) goes through one
+// shared-memory buffer that the two sides take in turn.
+//
+// Online softmax: the running max m of a row only moves when the tile maximum
+// exceeds it by more than 8 (a factor 256 in base 2); O and l are then scaled
+// by 2^(m_old - m_new).  Numerator and denominator use the same m, so the
+// result is exact for any m; the threshold only bounds P <= 256.  Scores are in
+// the log2 domain (scale pre-multiplied by log2 e).
+//
+// Every mbarrier wait is bounded (2 s); on expiry the kernel sets
+// PA_DEV_TIMEOUT, drains its in-flight copies and MMAs (bounded), frees TMEM
+// and exits.
 #include <cuda.h>
+#include <limits.h>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -46,86 +57,114 @@ using namespace tc;
 
 constexpr int kM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kN = 128;  // keys per tile
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 256 + D)
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 template <int D>
-struct TcLayout {
-  static constexpr int kHalves = D / 64;         // 64-element (128-byte) column chunks
-  static constexpr int kHalf = kM * 128;          // one chunk of a 128-row tile: 16 KB
-  static constexpr int kTile = kHalves * kHalf;   // Q, K or V tile
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;           // 2 stages
-  static constexpr int kV = kK + 2 * kTile;       // 2 stages
-  static constexpr int kP = kV + 2 * kTile;       // 128 rows x 128 keys: 2 chunks
+struct PpLayout {
+  static constexpr int kHalves = D / 64;        // 64-element (128-byte) column chunks
+  static constexpr int kHalf = kM * 128;         // one chunk of a 128-row tile: 16 KB
+  static constexpr int kTile = kHalves * kHalf;  // Q, K or V tile
+  static constexpr int kQA = 0;
+  static constexpr int kQB = kTile;
+  static constexpr int kK = 2 * kTile;           // 2 stages
+  static constexpr int kV = 4 * kTile;           // 2 stages
+  static constexpr int kP = 6 * kTile;           // 128 rows x 128 keys, shared by A and B
   static constexpr int kBar = kP + 2 * kHalf;
-  static constexpr int kBytes = kBar + 128;
-  static constexpr int kAlloc = kBytes + 1024;    // slack to align the base to 1 KB
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1 KB
 };
 
 enum : int {
-  kBarQ = 0,
-  kBarK0 = 1,  // K full, stages 0/1
-  kBarV0 = 3,  // V full
-  kBarE0 = 5,  // stage empty (PV done)
-  kBarS0 = 7,  // S buffer full
-  kBarP = 9,   // P written by the 128 softmax threads
-  kBarO = 10,  // PV done
-  kBarDrain = 11,
-  kNumBars = 12
+  bQFull, bQFree, bKFull0, bKFull1, bVFull0, bVFull1, bKEmpty0, bKEmpty1, bVEmpty0, bVEmpty1,
+  bSA, bSB, bPA, bPB, bPvA, bPvB, bOFreeA, bOFreeB, bDrain, kNumBars
 };
 
+struct Item {
+  int s, hk, h[2], t0, qn, c, i0, kv_end, n;  // h[1] < 0: no second tile
+};
+
+// Work slot e -> item.  Slots enumerate (tile counted from the end, sequence,
+// kv head, head pair); a slot whose tile does not exist is empty.
+__device__ bool decode_item(const AttnArgs& a, int e, int pairs, Item& it, bool& bad) {
+  const int S_pre = a.num_seqs - a.num_decode;
+  const int per_seq = a.hkv * pairs;
+  const int per_z = per_seq * S_pre;
+  const int z = e / per_z;
+  int rest = e - z * per_z;
+  const int sp = rest / per_seq;
+  rest -= sp * per_seq;
+  const int hk = rest / pairs;
+  const int p = rest - hk * pairs;
+  const int s = a.num_decode + sp;
+  const int t0 = __ldg(a.qsl + s);
+  const int qn = __ldg(a.qsl + s + 1) - t0;
+  const int L = __ldg(a.seq_lens + s);
+  bad = false;
+  if (qn <= 0) return false;
+  if (L < qn || L > (a.max_blocks << a.bs_log2) || qn > a.max_query_len || L > a.max_seq_len ||
+      t0 < 0 || t0 + qn > a.num_tokens) {
+    bad = true;
+    return false;
+  }
+  const int tile = (qn + kM - 1) / kM - 1 - z;
+  if (tile < 0) return false;
+  it.s = s;
+  it.hk = hk;
+  it.h[0] = hk * a.group + 2 * p;
+  it.h[1] = 2 * p + 1 < a.group ? it.h[0] + 1 : -1;
+  it.t0 = t0;
+  it.qn = qn;
+  it.c = L - qn;
+  it.i0 = tile * kM;
+  it.kv_end = it.c + min(qn, it.i0 + kM);
+  it.n = (it.kv_end + kN - 1) / kN;
+  return true;
+}
+
+// Slot of the k-th item of CTA `cta` among G CTAs (boustrophedon rounds).
+__device__ __forceinline__ int slot_of(int k, int cta, int G) {
+  return k * G + ((k & 1) ? (G - 1 - cta) : cta);
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
-  using Ly = TcLayout<D>;
+                      const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
+                      int total_slots) {
+  using Ly = PpLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (base - raw);
-
-  const int h = blockIdx.x;
-  const int s = a.num_decode + static_cast<int>(blockIdx.y);
-  const int g = a.group;
-  const int hk = h / g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int t0 = __ldg(a.qsl + s);
-  const int qn = __ldg(a.qsl + s + 1) - t0;
-  const int L = __ldg(a.seq_lens + s);
-  if (qn <= 0) return;
-  if (L < qn || L > (a.max_blocks << a.bs_log2) || qn > a.max_query_len || L > a.max_seq_len ||
-      t0 < 0 || t0 + qn > a.num_tokens) {
-    if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0) flag_error(a.err, PA_DEV_BAD_LEN);
-    return;
-  }
-  const int ntiles = (qn + kM - 1) / kM;
-  const int tile = ntiles - 1 - static_cast<int>(blockIdx.z);
-  if (tile < 0) return;
-  const int c = L - qn;
-  const int i0 = tile * kM;
-  const int i_hi = min(qn, i0 + kM) - 1;
-  const int kv_end = c + i_hi + 1;  // keys [0, kv_end) are visible to some row
-  const int n = (kv_end + kN - 1) / kN;
+  const int pairs = (a.group + 1) >> 1;
+  const int G = gridDim.x, cta = blockIdx.x;
 
   const uint32_t bar0 = base + Ly::kBar;
   const uint32_t tmem_slot = bar0 + 8 * kNumBars;
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sgen + Ly::kBar + 8 * kNumBars + 4);
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(sgen + Ly::kBar + 8 * kNumBars + 4);
 #define BAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
 
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(BAR(i), i == kBarP ? 128u : 1u);
+    for (int i = 0; i < kNumBars; ++i) {
+      const bool many = i == bPA || i == bPB || i == bOFreeA || i == bOFreeB;
+      mbar_init(BAR(i), many ? 128u : 1u);
+    }
     *abort_flag = 0u;
     fence_barrier_init();
   }
-  if (threadIdx.x == 128) {
+  if (threadIdx.x == 32 * kProducerWarp) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
@@ -139,235 +178,317 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 1u;
     flag_error(a.err, PA_DEV_TIMEOUT);
   };
+  auto wait = [&](int b, int completion) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait(BAR(b), static_cast<uint32_t>(completion) & 1u, kWaitNs)) return true;
+    give_up();
+    return false;
+  };
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const int32_t* bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks;
       const int bs = 1 << a.bs_log2;
-      const int R = bs < 128 ? bs : 128;  // cache rows per TMA box
-      mbar_expect_tx(BAR(kBarQ), Ly::kTile);
-#pragma unroll
-      for (int hf = 0; hf < Ly::kHalves; ++hf)
-        tma_load_2d(base + Ly::kQ + hf * Ly::kHalf, &tm_q, h * D + hf * 64, t0 + i0, BAR(kBarQ));
-      int issued_last = -1;
-      for (int j = 0; j < n; ++j) {
-        const int st = j & 1;
-        if (*abort_flag) break;
-        if (j >= 2 && !mbar_wait(BAR(kBarE0 + st), ((j >> 1) - 1) & 1, kWaitNs)) {
-          give_up();
-          break;
+      const int R = bs < kN ? bs : kN;  // cache rows per TMA box
+      int gt = 0, it = 0, last_k = -1, last_v = -1;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int e = slot_of(k, cta, G);
+        if (e >= total_slots) break;
+        Item I;
+        bool bad;
+        if (!decode_item(a, e, pairs, I, bad)) {
+          if (bad) flag_error(a.err, PA_DEV_BAD_LEN);
+          continue;
         }
-        const int p0 = j * kN;
-        const int p1 = min(kv_end, p0 + kN);
-        const int nbox = (p1 - p0 + R - 1) / R;
-        int slots[kN / 8];
-        int nvalid = 0;
-        for (int b = 0; b < nbox; ++b) {
-          const int pos = p0 + b * R;
-          const int pb = __ldg(bt + (pos >> a.bs_log2));
-          if (pb >= 0 && pb < a.num_blocks) {
-            slots[b] = (pb << a.bs_log2) + (pos & (bs - 1));
-            ++nvalid;
-          } else {
-            slots[b] = -1;
-            flag_error(a.err, PA_DEV_BAD_BLOCK);
+        if (it > 0 && !(ok = wait(bQFree, it - 1))) break;
+        const bool hasB = I.h[1] >= 0;
+        mbar_expect_tx(BAR(bQFull), Ly::kTile * (hasB ? 2 : 1));
+#pragma unroll
+        for (int hf = 0; hf < Ly::kHalves; ++hf) {
+          tma_load_2d(base + Ly::kQA + hf * Ly::kHalf, &tm_q, I.h[0] * D + hf * 64, I.t0 + I.i0,
+                      BAR(bQFull));
+          if (hasB)
+            tma_load_2d(base + Ly::kQB + hf * Ly::kHalf, &tm_q, I.h[1] * D + hf * 64,
+                        I.t0 + I.i0, BAR(bQFull));
+        }
+        ++it;
+        const int32_t* bt = a.block_tables + static_cast<int64_t>(I.s) * a.max_blocks;
+        for (int j = 0; j < I.n; ++j, ++gt) {
+          const int st = gt & 1;
+          const int p0 = j * kN;
+          const int nbox = (min(I.kv_end, p0 + kN) - p0 + R - 1) / R;
+          int slots[kN / 8];
+          int nvalid = 0;
+          for (int b = 0; b < nbox; ++b) {
+            const int pos = p0 + b * R;
+            const int pb = __ldg(bt + (pos >> a.bs_log2));
+            if (pb >= 0 && pb < a.num_blocks) {
+              slots[b] = (pb << a.bs_log2) + (pos & (bs - 1));
+              ++nvalid;
+            } else {
+              slots[b] = -1;
+              flag_error(a.err, PA_DEV_BAD_BLOCK);
+            }
           }
-        }
-        const uint32_t bytes = static_cast<uint32_t>(nvalid * R * 128 * Ly::kHalves);
-        const uint32_t kdst = base + Ly::kK + st * Ly::kTile;
-        const uint32_t vdst = base + Ly::kV + st * Ly::kTile;
-        mbar_expect_tx(BAR(kBarK0 + st), bytes);
-        for (int b = 0; b < nbox; ++b) {
-          if (slots[b] < 0) continue;
+          const uint32_t bytes = static_cast<uint32_t>(nvalid * R * 128 * Ly::kHalves);
+          if (gt >= 2 && !(ok = wait(bKEmpty0 + st, (gt >> 1) - 1))) break;
+          mbar_expect_tx(BAR(bKFull0 + st), bytes);
+          const uint32_t kdst = base + Ly::kK + st * Ly::kTile;
+          for (int b = 0; b < nbox; ++b) {
+            if (slots[b] < 0) continue;
 #pragma unroll
-          for (int hf = 0; hf < Ly::kHalves; ++hf)
-            tma_load_3d(kdst + hf * Ly::kHalf + b * R * 128, &tm_k, hf * 64, hk, slots[b],
-                        BAR(kBarK0 + st));
-        }
-        mbar_expect_tx(BAR(kBarV0 + st), bytes);
-        for (int b = 0; b < nbox; ++b) {
-          if (slots[b] < 0) continue;
+            for (int hf = 0; hf < Ly::kHalves; ++hf)
+              tma_load_3d(kdst + hf * Ly::kHalf + b * R * 128, &tm_k, hf * 64, I.hk, slots[b],
+                          BAR(bKFull0 + st));
+          }
+          last_k = gt;
+          if (gt >= 2 && !(ok = wait(bVEmpty0 + st, (gt >> 1) - 1))) break;
+          mbar_expect_tx(BAR(bVFull0 + st), bytes);
+          const uint32_t vdst = base + Ly::kV + st * Ly::kTile;
+          for (int b = 0; b < nbox; ++b) {
+            if (slots[b] < 0) continue;
 #pragma unroll
-          for (int hf = 0; hf < Ly::kHalves; ++hf)
-            tma_load_3d(vdst + hf * Ly::kHalf + b * R * 128, &tm_v, hf * 64, hk, slots[b],
-                        BAR(kBarV0 + st));
+            for (int hf = 0; hf < Ly::kHalves; ++hf)
+              tma_load_3d(vdst + hf * Ly::kHalf + b * R * 128, &tm_v, hf * 64, I.hk, slots[b],
+                          BAR(bVFull0 + st));
+          }
+          last_v = gt;
         }
-        issued_last = j;
       }
-      // drain: the last (up to) two tiles' copies must have landed before exit
-      for (int j = max(0, issued_last - 1); j <= issued_last; ++j) {
-        mbar_wait(BAR(kBarK0 + (j & 1)), (j >> 1) & 1, kWaitNs);
-        mbar_wait(BAR(kBarV0 + (j & 1)), (j >> 1) & 1, kWaitNs);
-      }
-      {
-        // the Q copy too
-        mbar_wait(BAR(kBarQ), 0, kWaitNs);
-      }
+      // drain: every copy this thread issued has landed before the CTA exits
+      for (int t = max(0, last_k - 1); t <= last_k; ++t)
+        mbar_wait(BAR(bKFull0 + (t & 1)), (t >> 1) & 1, kWaitNs);
+      for (int t = max(0, last_v - 1); t <= last_v; ++t)
+        mbar_wait(BAR(bVFull0 + (t & 1)), (t >> 1) & 1, kWaitNs);
+      if (it > 0) mbar_wait(BAR(bQFull), (it - 1) & 1, kWaitNs);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_bf16(kM, kN, false);
     constexpr uint32_t kIdO = idesc_bf16(kM, D, true);
-    const uint32_t tO = tmem + 256;
-    auto issue_s = [&](int j) {
-      const int st = j & 1;
-      const uint32_t q0 = base + Ly::kQ, k0 = base + Ly::kK + st * Ly::kTile;
+    auto issue_s = [&](int side, int g) {
+      const uint32_t q0 = base + (side ? Ly::kQB : Ly::kQA);
+      const uint32_t k0 = base + Ly::kK + (g & 1) * Ly::kTile;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * Ly::kHalf + (kk & 3) * 32;
-        mma_f16_ss(tmem + st * 128, smem_desc_sw128(q0 + off, 16, 1024),
+        mma_f16_ss(tmem + side * 128, smem_desc_sw128(q0 + off, 16, 1024),
                    smem_desc_sw128(k0 + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
       }
-      mma_commit(BAR(kBarS0 + st));
+      mma_commit(BAR(side ? bSB : bSA));
     };
-    bool ok = mbar_wait(BAR(kBarQ), 0, kWaitNs) && mbar_wait(BAR(kBarK0), 0, kWaitNs);
-    if (!ok) give_up();
-    tc_fence_after();
-    if (ok && lane == 0) issue_s(0);
-    __syncwarp();
-    for (int j = 0; ok && j < n; ++j) {
-      const int st = j & 1;
-      if (j + 1 < n) {
-        ok = !*abort_flag && mbar_wait(BAR(kBarK0 + ((j + 1) & 1)), ((j + 1) >> 1) & 1, kWaitNs);
+    auto issue_pv = [&](int side, int g, bool acc) {
+      const uint32_t p0 = base + Ly::kP;
+      const uint32_t v0 = base + Ly::kV + (g & 1) * Ly::kTile;
+#pragma unroll
+      for (int kk = 0; kk < kN / 16; ++kk) {
+        const uint32_t aoff = (kk >> 2) * Ly::kHalf + (kk & 3) * 32;
+        mma_f16_ss(tmem + 256 + side * 128, smem_desc_sw128(p0 + aoff, 16, 1024),
+                   smem_desc_sw128(v0 + kk * 2048, Ly::kHalf, 1024), kIdO,
+                   (acc || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(BAR(side ? bPvB : bPvA));
+    };
+    int gt = 0, it = 0, gB = 0, itB = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int e = slot_of(k, cta, G);
+      if (e >= total_slots) break;
+      Item I;
+      bool bad;
+      if (!decode_item(a, e, pairs, I, bad)) continue;
+      const bool hasB = I.h[1] >= 0;
+      if (!(ok = wait(bQFull, it) && wait(bKFull0 + (gt & 1), gt >> 1))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(0, gt);
+        if (hasB) issue_s(1, gt);
+        mma_commit(BAR(bKEmpty0 + (gt & 1)));
+      }
+      __syncwarp();
+      for (int j = 0; j < I.n; ++j) {
+        const int g = gt + j;
+        ok = wait(bPA, g) && (j > 0 || it == 0 || wait(bOFreeA, it - 1)) &&
+             wait(bVFull0 + (g & 1), g >> 1);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) issue_s(j + 1);
+        const int live = I.kv_end - j * kN;  // rows [live, 128) of V_j are not keys
+        if (live < kN) {
+          uint8_t* vt = sgen + Ly::kV + (g & 1) * Ly::kTile;
+          const int chunks = (kN - live) * 128 / 16;
+          for (int hf = 0; hf < Ly::kHalves; ++hf) {
+            uint4* p = reinterpret_cast<uint4*>(vt + hf * Ly::kHalf + live * 128);
+            for (int x = lane; x < chunks; x += 32) p[x] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) issue_pv(0, g, j > 0);
+        __syncwarp();
+        if (j + 1 < I.n) {
+          if (!(ok = wait(bKFull0 + ((g + 1) & 1), (g + 1) >> 1))) break;
+          tc_fence_after();
+          if (lane == 0) issue_s(0, g + 1);
+          __syncwarp();
+        }
+        if (hasB) {
+          if (!(ok = wait(bPB, gB + j) && (j > 0 || itB == 0 || wait(bOFreeB, itB - 1)))) break;
+          tc_fence_after();
+          if (lane == 0) {
+            issue_pv(1, g, j > 0);
+            if (j + 1 < I.n) issue_s(1, g + 1);
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          mma_commit(BAR(bVEmpty0 + (g & 1)));
+          if (j + 1 < I.n) mma_commit(BAR(bKEmpty0 + ((g + 1) & 1)));
+        }
         __syncwarp();
       }
-      ok = !*abort_flag && mbar_wait(BAR(kBarP), j & 1, kWaitNs) &&
-           mbar_wait(BAR(kBarV0 + st), (j >> 1) & 1, kWaitNs);
       if (!ok) break;
-      tc_fence_after();
-      const int live = kv_end - j * kN;  // rows [live, 128) of this V tile are not keys
-      if (live < kN) {
-        uint8_t* vt = sgen + Ly::kV + st * Ly::kTile;
-        const int nbytes = (kN - live) * 128;
-        for (int hf = 0; hf < Ly::kHalves; ++hf) {
-          uint4* p = reinterpret_cast<uint4*>(vt + hf * Ly::kHalf + live * 128);
-          for (int x = lane; x < nbytes / 16; x += 32) p[x] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-      }
+      if (lane == 0) mma_commit(BAR(bQFree));
       __syncwarp();
-      if (lane == 0) {
-        const uint32_t p0 = base + Ly::kP, v0 = base + Ly::kV + st * Ly::kTile;
-#pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * Ly::kHalf + (kk & 3) * 32;
-          mma_f16_ss(tO, smem_desc_sw128(p0 + aoff, 16, 1024),
-                     smem_desc_sw128(v0 + kk * 2048, Ly::kHalf, 1024), kIdO,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(BAR(kBarO));
-        mma_commit(BAR(kBarE0 + st));
+      gt += I.n;
+      ++it;
+      if (hasB) {
+        gB += I.n;
+        ++itB;
       }
-      __syncwarp();
     }
-    if (!ok) give_up();
-    // drain: every MMA this thread issued has completed once this arrives
-    if (lane == 0) mma_commit(BAR(kBarDrain));
+    if (lane == 0) mma_commit(BAR(bDrain));
     __syncwarp();
-    mbar_wait(BAR(kBarDrain), 0, kWaitNs);
+    mbar_wait(BAR(bDrain), 0, kWaitNs);
   } else {
-    // ------------------------------------------------------------ softmax
-    const int r = threadIdx.x;  // 0..127
-    const int i = i0 + r;
-    const bool row_ok = i < qn;
-    const int lim = c + i;  // last key position this row sees
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax A / B
+    const int side = warp >> 2;  // 0: A (warps 0-3), 1: B (warps 4-7)
+    const int r = threadIdx.x - side * 128;  // query row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + side * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + side * 128 + lane_off;
     const uint32_t prow = base + Ly::kP + r * 128;
-    float m_used = -INFINITY, l = 0.f;
+    int gt = 0, gx = 0, nB = 0;  // all tiles, this side's tiles, B tiles so far
+    bool prev_hasB = false;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      ok = !*abort_flag && mbar_wait(BAR(kBarS0 + (j & 1)), (j >> 1) & 1, kWaitNs);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
+    for (int k = 0; ok; ++k) {
+      const int e = slot_of(k, cta, G);
+      if (e >= total_slots) break;
+      Item I;
+      bool bad;
+      if (!decode_item(a, e, pairs, I, bad)) continue;
+      const bool hasB = I.h[1] >= 0;
+      if (side == 1 && !hasB) {
+        gt += I.n;
+        prev_hasB = false;
+        continue;
+      }
+      const int i = I.i0 + r;
+      const bool row_ok = i < I.qn;
+      const int lim = I.c + i;  // last key position this row sees
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < I.n; ++j) {
+        const int g = gt + j;
+        if (!(ok = wait(side ? bSB : bSA, gx + j))) break;
+        tc_fence_after();
+        uint32_t sr[4][32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_off + (j & 1) * 128 + cc * 32, sr[cc]);
-      tmem_wait_ld();
-      const int key0 = j * kN;
-      const bool full = key0 + kN - 1 <= lim && key0 + kN <= kv_end;
-      float mt = -INFINITY;
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+        tmem_wait_ld();
+        const int key0 = j * kN;
+        const bool full = key0 + kN - 1 <= lim && key0 + kN <= I.kv_end;
+        float mx[8];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+        for (int x = 0; x < 8; ++x) mx[x] = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float v = __uint_as_float(sr[cc][e]) * a.scale_log2;
-          const int pos = key0 + cc * 32 + e;
-          if (!full && (pos > lim || pos >= kv_end)) v = -INFINITY;
-          sr[cc][e] = __float_as_uint(v);
-          mt = fmaxf(mt, v);
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int e2 = 0; e2 < 32; ++e2) {
+            float v = __uint_as_float(sr[cc][e2]) * a.scale_log2;
+            const int pos = key0 + cc * 32 + e2;
+            if (!full && (pos > lim || pos >= I.kv_end)) v = -INFINITY;
+            sr[cc][e2] = __float_as_uint(v);
+            mx[e2 & 7] = fmaxf(mx[e2 & 7], v);
+          }
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_new = mt > m_used + 8.f ? mt : m_used;
+        const float ref = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - ref);
+        float sm[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) sm[x] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int e2 = 0; e2 < 32; ++e2) {
+            const float p = ex2(__uint_as_float(sr[cc][e2]) - ref);
+            sm[e2 & 7] += p;
+            sr[cc][e2] = __float_as_uint(p);
+          }
+        l = l * alpha + (((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7])));
+        // the shared P buffer and this side's O must be free: wait for the
+        // last product issued before ours
+        if (side == 0) {
+          if (g > 0) {
+            if (prev_hasB) ok = wait(bPvB, nB - 1);
+            else ok = wait(bPvA, g - 1);
+          }
+        } else {
+          ok = wait(bPvA, g);
         }
-      const float m_new = mt > m_used + 8.f ? mt : m_used;
-      const float ref = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - ref);
-      float rs = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p = ex2(__uint_as_float(sr[cc][e]) - ref);
-          rs += p;
-          sr[cc][e] = __float_as_uint(p);
-        }
-      l = l * alpha + rs;
-      if (j > 0) {
-        ok = !*abort_flag && mbar_wait(BAR(kBarO), (j - 1) & 1, kWaitNs);
         if (!ok) break;
         tc_fence_after();
-      }
-      const bool need = j > 0 && m_new != m_used;
-      if (__any_sync(0xffffffffu, need)) {
-        const float f = need ? alpha : 1.f;
+        const bool need = j > 0 && m_new != m_used;
+        if (__any_sync(0xffffffffu, need)) {
+          const float f = need ? alpha : 1.f;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + 256 + cc * 32, o);
-          tmem_wait_ld();
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-          tmem_st32(tmem + lane_off + 256 + cc * 32, o);
+            for (int e2 = 0; e2 < 32; ++e2) o[e2] = __float_as_uint(__uint_as_float(o[e2]) * f);
+            tmem_st32(tO + cc * 32, o);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
+        m_used = m_new;
+        // P row -> smem, K-major with the 128-byte swizzle: 16-byte chunk q of
+        // row r in a 64-key half lands at chunk q ^ (r & 7).
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) {
+            const int kx = hf * 64 + q8 * 8;
+            const uint32_t* v = &sr[kx >> 5][kx & 31];
+            const uint32_t w0 = pack_bf16(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            const uint32_t w1 = pack_bf16(__uint_as_float(v[2]), __uint_as_float(v[3]));
+            const uint32_t w2 = pack_bf16(__uint_as_float(v[4]), __uint_as_float(v[5]));
+            const uint32_t w3 = pack_bf16(__uint_as_float(v[6]), __uint_as_float(v[7]));
+            const uint32_t addr = prow + hf * Ly::kHalf + ((q8 ^ (r & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(w0),
+                         "r"(w1), "r"(w2), "r"(w3)
+                         : "memory");
+          }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(BAR(side ? bPB : bPA));
+        prev_hasB = hasB;
+        if (hasB) ++nB;
       }
-      m_used = m_new;
-      // P row -> smem, K-major with the 128-byte swizzle: 16-byte chunk q of
-      // row r in a 64-key half lands at chunk q ^ (r & 7).
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-          const int k = hf * 64 + q8 * 8;
-          const uint32_t* v = &sr[k >> 5][k & 31];
-          uint4 w;
-          w.x = pack_bf16(__uint_as_float(v[0]), __uint_as_float(v[1]));
-          w.y = pack_bf16(__uint_as_float(v[2]), __uint_as_float(v[3]));
-          w.z = pack_bf16(__uint_as_float(v[4]), __uint_as_float(v[5]));
-          w.w = pack_bf16(__uint_as_float(v[6]), __uint_as_float(v[7]));
-          const uint32_t addr = prow + hf * Ly::kHalf + ((q8 ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(w.x),
-                       "r"(w.y), "r"(w.z), "r"(w.w)
-                       : "memory");
-        }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(BAR(kBarP));
-    }
-    if (ok) ok = !*abort_flag && mbar_wait(BAR(kBarO), (n - 1) & 1, kWaitNs);
-    if (!ok) {
-      give_up();
-    } else {
+      if (!ok) break;
+      // epilogue: wait for this side's last product, normalise, store
+      if (!(ok = side == 0 ? wait(bPvA, gt + I.n - 1) : wait(bPvB, nB - 1))) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                            static_cast<int64_t>(t0 + (row_ok ? i : 0)) * a.out_stride +
-                            static_cast<int64_t>(h) * D;
+                            static_cast<int64_t>(I.t0 + (row_ok ? i : 0)) * a.out_stride +
+                            static_cast<int64_t>(I.h[side]) * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + 256 + cc * 32, o);
+        tmem_ld32(tO + cc * 32, o);
         tmem_wait_ld();
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
@@ -382,12 +503,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(BAR(side ? bOFreeB : bOFreeA));
+      gt += I.n;
+      gx += I.n;
     }
   }
 #undef BAR
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -442,9 +567,15 @@ bool encode_cache(CUtensorMap* m, const void* ptr, const AttnArgs& a) {
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int64_t total_slots_of(const AttnArgs& a) {
+  const int64_t pairs = (a.group + 1) / 2;
+  const int64_t tiles = (static_cast<int64_t>(a.max_query_len) + kM - 1) / kM;
+  return static_cast<int64_t>(a.hkv) * pairs * (a.num_seqs - a.num_decode) * tiles;
+}
+
 template <int D>
 cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
-  using Ly = TcLayout<D>;
+  using Ly = PpLayout<D>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -457,9 +588,12 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!encode_q(&mq, a) || !encode_cache(&mk, a.k_cache, a) || !encode_cache(&mv, a.v_cache, a))
     return cudaErrorNotSupported;  // nothing launched: the caller takes the general kernel
-  dim3 grid(a.hq, a.num_seqs - a.num_decode, (a.max_query_len + kM - 1) / kM);
+  const int total = static_cast<int>(total_slots_of(a));
+  const int sms = device_num_sms();
+  const int grid = total < sms ? total : sms;
+  if (grid <= 0) return cudaSuccess;
   count_launch();
-  prefill_tc_kernel<D><<<grid, kThreads, Ly::kAlloc, st>>>(mq, mk, mv, a);
+  prefill_tc_kernel<D><<<grid, kThreads, Ly::kAlloc, st>>>(mq, mk, mv, a, total);
   return cudaGetLastError();
 }
 
@@ -474,7 +608,7 @@ bool prefill_tc_supported(const AttnArgs& a) {
   if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k_cache) |
        reinterpret_cast<uintptr_t>(a.v_cache)) & 15u)
     return false;
-  if ((a.max_query_len + kM - 1) / kM > 65535) return false;
+  if (total_slots_of(a) > INT_MAX / 2) return false;
   return encode_fn() != nullptr;
 }
 
