@@ -132,7 +132,7 @@ __device__ __forceinline__ int slot_of(int k, int cta, int G) {
 }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
@@ -391,41 +391,58 @@ __global__ void __maxnreg__(200)
         const int g = gt + j;
         if (!(ok = wait(side ? bSB : bSA, gx + j))) break;
         tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
-        tmem_wait_ld();
         const int key0 = j * kN;
         const bool full = key0 + kN - 1 <= lim && key0 + kN <= I.kv_end;
+        // pass 1: row maximum of the scaled, masked scores (two 64-column loads)
         float mx[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) mx[x] = -INFINITY;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sr[2][32];
+          tmem_ld32(tS + hh * 64, sr[0]);
+          tmem_ld32(tS + hh * 64 + 32, sr[1]);
+          tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-          for (int e2 = 0; e2 < 32; ++e2) {
-            float v = __uint_as_float(sr[cc][e2]) * a.scale_log2;
-            const int pos = key0 + cc * 32 + e2;
-            if (!full && (pos > lim || pos >= I.kv_end)) v = -INFINITY;
-            sr[cc][e2] = __float_as_uint(v);
-            mx[e2 & 7] = fmaxf(mx[e2 & 7], v);
-          }
+            for (int e2 = 0; e2 < 32; ++e2) {
+              float v = __uint_as_float(sr[cc][e2]) * a.scale_log2;
+              const int pos = key0 + hh * 64 + cc * 32 + e2;
+              if (!full && (pos > lim || pos >= I.kv_end)) v = -INFINITY;
+              mx[e2 & 7] = fmaxf(mx[e2 & 7], v);
+            }
+        }
         const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = mt > m_used + 8.f ? mt : m_used;
         const float ref = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - ref);
+        // pass 2: P = 2^(s - m) (bf16, packed in pairs) and the row sum
+        uint32_t pk[64];
         float sm[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) sm[x] = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t sr[32];
+          tmem_ld32(tS + cc * 32, sr);
+          tmem_wait_ld();
 #pragma unroll
-          for (int e2 = 0; e2 < 32; ++e2) {
-            const float p = ex2(__uint_as_float(sr[cc][e2]) - ref);
-            sm[e2 & 7] += p;
-            sr[cc][e2] = __float_as_uint(p);
+          for (int e2 = 0; e2 < 32; e2 += 2) {
+            float v0 = __uint_as_float(sr[e2]) * a.scale_log2 - ref;
+            float v1 = __uint_as_float(sr[e2 + 1]) * a.scale_log2 - ref;
+            if (!full) {
+              const int pos = key0 + cc * 32 + e2;
+              if (pos > lim || pos >= I.kv_end) v0 = -INFINITY;
+              if (pos + 1 > lim || pos + 1 >= I.kv_end) v1 = -INFINITY;
+            }
+            const float p0 = ex2(v0), p1 = ex2(v1);
+            sm[e2 & 7] += p0;
+            sm[(e2 + 1) & 7] += p1;
+            pk[cc * 16 + (e2 >> 1)] = pack_bf16(p0, p1);
           }
+        }
         l = l * alpha + (((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7])));
         // the shared P buffer and this side's O must be free: wait for the
         // last product issued before ours
@@ -460,15 +477,10 @@ __global__ void __maxnreg__(200)
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
           for (int q8 = 0; q8 < 8; ++q8) {
-            const int kx = hf * 64 + q8 * 8;
-            const uint32_t* v = &sr[kx >> 5][kx & 31];
-            const uint32_t w0 = pack_bf16(__uint_as_float(v[0]), __uint_as_float(v[1]));
-            const uint32_t w1 = pack_bf16(__uint_as_float(v[2]), __uint_as_float(v[3]));
-            const uint32_t w2 = pack_bf16(__uint_as_float(v[4]), __uint_as_float(v[5]));
-            const uint32_t w3 = pack_bf16(__uint_as_float(v[6]), __uint_as_float(v[7]));
+            const uint32_t* w = &pk[hf * 32 + q8 * 4];  // keys hf*64 + q8*8 .. +7
             const uint32_t addr = prow + hf * Ly::kHalf + ((q8 ^ (r & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(w0),
-                         "r"(w1), "r"(w2), "r"(w3)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(w[0]),
+                         "r"(w[1]), "r"(w[2]), "r"(w[3])
                          : "memory");
           }
         fence_proxy_async_smem();
