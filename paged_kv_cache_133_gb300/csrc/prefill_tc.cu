@@ -14,11 +14,17 @@
 // walk the item list in a boustrophedon order over "tile counted from the
 // end of its sequence", so the longest key ranges start first.
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
 //   warps 4-7  softmax + epilogue of tile B
-//   warp 8     TMA producer: Q_A/Q_B per item, K_j and V_j into 2-stage rings
+//   warp 8     TMA producer: Q_A/Q_B per item, K_j and V_j into 2-stage rings;
+//              its 32 lanes resolve a tile's blocks and issue their boxes in parallel
 //   warp 9     TMEM allocation and MMA issue (one lane)
+//   warps 10-11 idle (they complete the third warpgroup)
+// The softmax warpgroups raise their register limit to 200 and the third
+// warpgroup lowers its to 96 (256*200 + 128*96 = 63488 <= 384*168 launched;
+// per SM sub-partition 200+200+96 registers x 32 lanes <= 16384), so a softmax
+// thread holds its whole 128-score row after one TMEM load.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Per key tile j the tensor core runs, in issue order,
 //   PV_A(j-1) .. S_A(j) .. PV_B(j-1) .. S_B(j) ..
@@ -60,7 +66,7 @@ constexpr int kN = 128;  // keys per tile
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -185,24 +191,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     return false;
   };
 
+  if (warp >= kProducerWarp) regs_decrease<96>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const int bs = 1 << a.bs_log2;
-      const int R = bs < kN ? bs : kN;  // cache rows per TMA box
-      int gt = 0, it = 0, last_k = -1, last_v = -1;
-      bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int e = slot_of(k, cta, G);
-        if (e >= total_slots) break;
-        Item I;
-        bool bad;
-        if (!decode_item(a, e, pairs, I, bad)) {
-          if (bad) flag_error(a.err, PA_DEV_BAD_LEN);
-          continue;
-        }
-        if (it > 0 && !(ok = wait(bQFree, it - 1))) break;
-        const bool hasB = I.h[1] >= 0;
+    const int bs = 1 << a.bs_log2;
+    const int R = bs < kN ? bs : kN;  // cache rows per TMA box; lane b owns box b
+    int gt = 0, it = 0, last_k = -1, last_v = -1;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int e = slot_of(k, cta, G);
+      if (e >= total_slots) break;
+      Item I;
+      bool bad;
+      if (!decode_item(a, e, pairs, I, bad)) {
+        if (bad && lane == 0) flag_error(a.err, PA_DEV_BAD_LEN);
+        continue;
+      }
+      if (it > 0 && !(ok = wait(bQFree, it - 1))) break;
+      const bool hasB = I.h[1] >= 0;
+      if (lane == 0) {
         mbar_expect_tx(BAR(bQFull), Ly::kTile * (hasB ? 2 : 1));
 #pragma unroll
         for (int hf = 0; hf < Ly::kHalves; ++hf) {
@@ -212,57 +219,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(base + Ly::kQB + hf * Ly::kHalf, &tm_q, I.h[1] * D + hf * 64,
                         I.t0 + I.i0, BAR(bQFull));
         }
-        ++it;
-        const int32_t* bt = a.block_tables + static_cast<int64_t>(I.s) * a.max_blocks;
-        for (int j = 0; j < I.n; ++j, ++gt) {
-          const int st = gt & 1;
-          const int p0 = j * kN;
-          const int nbox = (min(I.kv_end, p0 + kN) - p0 + R - 1) / R;
-          int slots[kN / 8];
-          int nvalid = 0;
-          for (int b = 0; b < nbox; ++b) {
-            const int pos = p0 + b * R;
-            const int pb = __ldg(bt + (pos >> a.bs_log2));
-            if (pb >= 0 && pb < a.num_blocks) {
-              slots[b] = (pb << a.bs_log2) + (pos & (bs - 1));
-              ++nvalid;
-            } else {
-              slots[b] = -1;
-              flag_error(a.err, PA_DEV_BAD_BLOCK);
-            }
-          }
-          const uint32_t bytes = static_cast<uint32_t>(nvalid * R * 128 * Ly::kHalves);
-          if (gt >= 2 && !(ok = wait(bKEmpty0 + st, (gt >> 1) - 1))) break;
-          mbar_expect_tx(BAR(bKFull0 + st), bytes);
-          const uint32_t kdst = base + Ly::kK + st * Ly::kTile;
-          for (int b = 0; b < nbox; ++b) {
-            if (slots[b] < 0) continue;
-#pragma unroll
-            for (int hf = 0; hf < Ly::kHalves; ++hf)
-              tma_load_3d(kdst + hf * Ly::kHalf + b * R * 128, &tm_k, hf * 64, I.hk, slots[b],
-                          BAR(bKFull0 + st));
-          }
-          last_k = gt;
-          if (gt >= 2 && !(ok = wait(bVEmpty0 + st, (gt >> 1) - 1))) break;
-          mbar_expect_tx(BAR(bVFull0 + st), bytes);
-          const uint32_t vdst = base + Ly::kV + st * Ly::kTile;
-          for (int b = 0; b < nbox; ++b) {
-            if (slots[b] < 0) continue;
-#pragma unroll
-            for (int hf = 0; hf < Ly::kHalves; ++hf)
-              tma_load_3d(vdst + hf * Ly::kHalf + b * R * 128, &tm_v, hf * 64, I.hk, slots[b],
-                          BAR(bVFull0 + st));
-          }
-          last_v = gt;
-        }
       }
-      // drain: every copy this thread issued has landed before the CTA exits
+      ++it;
+      const int32_t* bt = a.block_tables + static_cast<int64_t>(I.s) * a.max_blocks;
+      for (int j = 0; j < I.n; ++j, ++gt) {
+        const int st = gt & 1;
+        const int p0 = j * kN;
+        const int nbox = (min(I.kv_end, p0 + kN) - p0 + R - 1) / R;
+        int slot = -1;
+        if (lane < nbox) {
+          const int pos = p0 + lane * R;
+          const int pb = __ldg(bt + (pos >> a.bs_log2));
+          if (pb >= 0 && pb < a.num_blocks) slot = (pb << a.bs_log2) + (pos & (bs - 1));
+          else flag_error(a.err, PA_DEV_BAD_BLOCK);
+        }
+        const uint32_t valid = __ballot_sync(0xffffffffu, slot >= 0);
+        const uint32_t bytes = static_cast<uint32_t>(__popc(valid) * R * 128 * Ly::kHalves);
+        if (gt >= 2 && !(ok = wait(bKEmpty0 + st, (gt >> 1) - 1))) break;
+        if (lane == 0) mbar_expect_tx(BAR(bKFull0 + st), bytes);
+        __syncwarp();
+        if (slot >= 0) {
+          const uint32_t kdst = base + Ly::kK + st * Ly::kTile + lane * R * 128;
+#pragma unroll
+          for (int hf = 0; hf < Ly::kHalves; ++hf)
+            tma_load_3d(kdst + hf * Ly::kHalf, &tm_k, hf * 64, I.hk, slot, BAR(bKFull0 + st));
+        }
+        last_k = gt;
+        if (gt >= 2 && !(ok = wait(bVEmpty0 + st, (gt >> 1) - 1))) break;
+        if (lane == 0) mbar_expect_tx(BAR(bVFull0 + st), bytes);
+        __syncwarp();
+        if (slot >= 0) {
+          const uint32_t vdst = base + Ly::kV + st * Ly::kTile + lane * R * 128;
+#pragma unroll
+          for (int hf = 0; hf < Ly::kHalves; ++hf)
+            tma_load_3d(vdst + hf * Ly::kHalf, &tm_v, hf * 64, I.hk, slot, BAR(bVFull0 + st));
+        }
+        last_v = gt;
+      }
+    }
+    // drain: every copy this warp issued has landed before the CTA exits
+    if (lane == 0) {
       for (int t = max(0, last_k - 1); t <= last_k; ++t)
         mbar_wait(BAR(bKFull0 + (t & 1)), (t >> 1) & 1, kWaitNs);
       for (int t = max(0, last_v - 1); t <= last_v; ++t)
         mbar_wait(BAR(bVFull0 + (t & 1)), (t >> 1) & 1, kWaitNs);
       if (it > 0) mbar_wait(BAR(bQFull), (it - 1) & 1, kWaitNs);
     }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_bf16(kM, kN, false);
@@ -360,8 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mma_commit(BAR(bDrain));
     __syncwarp();
     mbar_wait(BAR(bDrain), 0, kWaitNs);
-  } else {
+  } else if (warp < kProducerWarp) {
     // ------------------------------------------------------------ softmax A / B
+    regs_increase<200>();
     const int side = warp >> 2;  // 0: A (warps 0-3), 1: B (warps 4-7)
     const int r = threadIdx.x - side * 128;  // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -393,23 +397,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int key0 = j * kN;
         const bool full = key0 + kN - 1 <= lim && key0 + kN <= I.kv_end;
-        // pass 1: row maximum of the scaled, masked scores (two 64-column loads)
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+        tmem_wait_ld();
         float mx[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) mx[x] = -INFINITY;
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sr[2][32];
-          tmem_ld32(tS + hh * 64, sr[0]);
-          tmem_ld32(tS + hh * 64 + 32, sr[1]);
-          tmem_wait_ld();
+        if (full) {
+          // every key of the tile is visible: scores stay raw, the scale is
+          // folded into the exponent below (max commutes with a positive scale)
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
+          for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
             for (int e2 = 0; e2 < 32; ++e2) {
+              const float v = __uint_as_float(sr[cc][e2]) * a.scale_log2;
+              mx[e2 & 7] = fmaxf(mx[e2 & 7], v);
+            }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+            for (int e2 = 0; e2 < 32; ++e2) {
+              const int pos = key0 + cc * 32 + e2;
               float v = __uint_as_float(sr[cc][e2]) * a.scale_log2;
-              const int pos = key0 + hh * 64 + cc * 32 + e2;
-              if (!full && (pos > lim || pos >= I.kv_end)) v = -INFINITY;
+              if (pos > lim || pos >= I.kv_end) v = -INFINITY;
+              sr[cc][e2] = __float_as_uint(v);
               mx[e2 & 7] = fmaxf(mx[e2 & 7], v);
             }
         }
@@ -418,31 +431,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = mt > m_used + 8.f ? mt : m_used;
         const float ref = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - ref);
-        // pass 2: P = 2^(s - m) (bf16, packed in pairs) and the row sum
-        uint32_t pk[64];
+        // P = 2^(s - m), rounded to bf16 and packed in pairs into sr[0..1]
+        const float mul = full ? a.scale_log2 : 1.f;
         float sm[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) sm[x] = 0.f;
+        uint32_t* flat = &sr[0][0];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t sr[32];
-          tmem_ld32(tS + cc * 32, sr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e2 = 0; e2 < 32; e2 += 2) {
-            float v0 = __uint_as_float(sr[e2]) * a.scale_log2 - ref;
-            float v1 = __uint_as_float(sr[e2 + 1]) * a.scale_log2 - ref;
-            if (!full) {
-              const int pos = key0 + cc * 32 + e2;
-              if (pos > lim || pos >= I.kv_end) v0 = -INFINITY;
-              if (pos + 1 > lim || pos + 1 >= I.kv_end) v1 = -INFINITY;
-            }
-            const float p0 = ex2(v0), p1 = ex2(v1);
-            sm[e2 & 7] += p0;
-            sm[(e2 + 1) & 7] += p1;
-            pk[cc * 16 + (e2 >> 1)] = pack_bf16(p0, p1);
-          }
+        for (int e2 = 0; e2 < 128; e2 += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(flat[e2]), mul, -ref));
+          const float p1 = ex2(fmaf(__uint_as_float(flat[e2 + 1]), mul, -ref));
+          sm[e2 & 7] += p0;
+          sm[(e2 + 1) & 7] += p1;
+          flat[e2 >> 1] = pack_bf16(p0, p1);
         }
+        const uint32_t* pk = flat;
         l = l * alpha + (((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7])));
         // the shared P buffer and this side's O must be free: wait for the
         // last product issued before ours
