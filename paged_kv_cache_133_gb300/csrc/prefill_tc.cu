@@ -15,25 +15,30 @@
 // end of its sequence", so the longest key ranges start first.
 //
 // Warp roles (384 threads, three warpgroups):
-//   warps 0-3  softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
-//   warps 4-7  softmax + epilogue of tile B
-//   warp 8     TMA producer: Q_A/Q_B per item, K_j and V_j into 2-stage rings;
-//              its 32 lanes resolve a tile's blocks and issue their boxes in parallel
-//   warp 9     TMEM allocation and MMA issue (one lane)
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warps 0-3   softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
+//   warps 4-7   softmax + epilogue of tile B
+//   warp 8      TMA producer of Q_A/Q_B (per item) and K_j (3-stage ring)
+//   warp 9      TMEM allocation and MMA issue (one lane)
+//   warp 10     TMA producer of V_j (2-stage ring)
+//   warp 11     idle (completes the third warpgroup)
+// The producers' 32 lanes resolve a tile's blocks through the block table and
+// issue one TMA box each, in parallel.
 // The softmax warpgroups raise their register limit to 200 and the third
 // warpgroup lowers its to 96 (256*200 + 128*96 = 63488 <= 384*168 launched;
 // per SM sub-partition 200+200+96 registers x 32 lanes <= 16384), so a softmax
 // thread holds its whole 128-score row after one TMEM load.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
-// Per key tile j the tensor core runs, in issue order,
-//   PV_A(j-1) .. S_A(j) .. PV_B(j-1) .. S_B(j) ..
-// so while softmax A works on S_A(j) the tensor core computes B's products and
-// the other way round (the two tiles ping-pong).  S = Q K^T and O += P V are
-// tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) with operands in 128-byte-
-// swizzled shared memory; V is read MN-major.  P (bf16) goes through one
-// shared-memory buffer that the two sides take in turn.
-//
+// P (bf16, two per 32-bit column) is written over the first 64 columns of its
+// own S and read from there as the A operand of O += P V.  Per key tile j the
+// tensor core runs, in issue order, PV_A(j) S_A(j+1) PV_B(j) S_B(j+1), so while
+// softmax A works on S_A(j+1) it computes B's products and the other way round
+// (the two tiles ping-pong).  tcgen05.mma operations issued by one thread run
+// in order, so S(j+1) overwrites P(j) only after PV(j) has read it, and the
+// commit that reports S(j+1) also reports every earlier product: a softmax
+// thread that has S(j+1) may rewrite its P columns and rescale its O.
+// S = Q K^T reads both operands from 128-byte-swizzled shared memory; V is read
+// MN-major.
+
 // Online softmax: the running max m of a row only moves when the tile maximum
 // exceeds it by more than 8 (a factor 256 in base 2); O and l are then scaled
 // by 2^(m_old - m_new).  Numerator and denominator use the same m, so the
@@ -66,6 +71,7 @@ constexpr int kN = 128;  // keys per tile
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kVWarp = 10;
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -75,18 +81,21 @@ struct PpLayout {
   static constexpr int kHalves = D / 64;        // 64-element (128-byte) column chunks
   static constexpr int kHalf = kM * 128;         // one chunk of a 128-row tile: 16 KB
   static constexpr int kTile = kHalves * kHalf;  // Q, K or V tile
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
   static constexpr int kQA = 0;
   static constexpr int kQB = kTile;
-  static constexpr int kK = 2 * kTile;           // 2 stages
-  static constexpr int kV = 4 * kTile;           // 2 stages
-  static constexpr int kP = 6 * kTile;           // 128 rows x 128 keys, shared by A and B
-  static constexpr int kBar = kP + 2 * kHalf;
+  static constexpr int kK = 2 * kTile;
+  static constexpr int kV = kK + kKStages * kTile;
+  static constexpr int kBar = kV + kVStages * kTile;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1 KB
 };
 
 enum : int {
-  bQFull, bQFree, bKFull0, bKFull1, bVFull0, bVFull1, bKEmpty0, bKEmpty1, bVEmpty0, bVEmpty1,
+  bQFull, bQFree,
+  bKFull0, bKFull1, bKFull2, bKEmpty0, bKEmpty1, bKEmpty2,
+  bVFull0, bVFull1, bVEmpty0, bVEmpty1,
   bSA, bSB, bPA, bPB, bPvA, bPvB, bOFreeA, bOFreeB, bDrain, kNumBars
 };
 
@@ -192,11 +201,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp >= kProducerWarp) regs_decrease<96>();
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
+  if (warp == kProducerWarp || warp == kVWarp) {
+    // ------------------------------------------------------------ producers
+    // warp 8: Q per item and the K tiles; warp 10: the V tiles.
+    const bool is_k = warp == kProducerWarp;
+    const int nst = is_k ? Ly::kKStages : Ly::kVStages;
+    const int full0 = is_k ? bKFull0 : bVFull0;
+    const int empty0 = is_k ? bKEmpty0 : bVEmpty0;
+    const uint32_t ring = base + (is_k ? Ly::kK : Ly::kV);
+    const CUtensorMap* map = is_k ? &tm_k : &tm_v;
     const int bs = 1 << a.bs_log2;
     const int R = bs < kN ? bs : kN;  // cache rows per TMA box; lane b owns box b
-    int gt = 0, it = 0, last_k = -1, last_v = -1;
+    int gt = 0, it = 0, last = -1;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int e = slot_of(k, cta, G);
@@ -204,26 +220,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item I;
       bool bad;
       if (!decode_item(a, e, pairs, I, bad)) {
-        if (bad && lane == 0) flag_error(a.err, PA_DEV_BAD_LEN);
+        if (bad && is_k && lane == 0) flag_error(a.err, PA_DEV_BAD_LEN);
         continue;
       }
-      if (it > 0 && !(ok = wait(bQFree, it - 1))) break;
-      const bool hasB = I.h[1] >= 0;
-      if (lane == 0) {
-        mbar_expect_tx(BAR(bQFull), Ly::kTile * (hasB ? 2 : 1));
+      if (is_k) {
+        if (it > 0 && !(ok = wait(bQFree, it - 1))) break;
+        if (lane == 0) {
+          const bool hasB = I.h[1] >= 0;
+          mbar_expect_tx(BAR(bQFull), Ly::kTile * (hasB ? 2 : 1));
 #pragma unroll
-        for (int hf = 0; hf < Ly::kHalves; ++hf) {
-          tma_load_2d(base + Ly::kQA + hf * Ly::kHalf, &tm_q, I.h[0] * D + hf * 64, I.t0 + I.i0,
-                      BAR(bQFull));
-          if (hasB)
-            tma_load_2d(base + Ly::kQB + hf * Ly::kHalf, &tm_q, I.h[1] * D + hf * 64,
+          for (int hf = 0; hf < Ly::kHalves; ++hf) {
+            tma_load_2d(base + Ly::kQA + hf * Ly::kHalf, &tm_q, I.h[0] * D + hf * 64,
                         I.t0 + I.i0, BAR(bQFull));
+            if (hasB)
+              tma_load_2d(base + Ly::kQB + hf * Ly::kHalf, &tm_q, I.h[1] * D + hf * 64,
+                          I.t0 + I.i0, BAR(bQFull));
+          }
         }
       }
       ++it;
       const int32_t* bt = a.block_tables + static_cast<int64_t>(I.s) * a.max_blocks;
       for (int j = 0; j < I.n; ++j, ++gt) {
-        const int st = gt & 1;
+        const int st = gt % nst;
         const int p0 = j * kN;
         const int nbox = (min(I.kv_end, p0 + kN) - p0 + R - 1) / R;
         int slot = -1;
@@ -231,39 +249,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pos = p0 + lane * R;
           const int pb = __ldg(bt + (pos >> a.bs_log2));
           if (pb >= 0 && pb < a.num_blocks) slot = (pb << a.bs_log2) + (pos & (bs - 1));
-          else flag_error(a.err, PA_DEV_BAD_BLOCK);
+          else if (is_k) flag_error(a.err, PA_DEV_BAD_BLOCK);
         }
         const uint32_t valid = __ballot_sync(0xffffffffu, slot >= 0);
         const uint32_t bytes = static_cast<uint32_t>(__popc(valid) * R * 128 * Ly::kHalves);
-        if (gt >= 2 && !(ok = wait(bKEmpty0 + st, (gt >> 1) - 1))) break;
-        if (lane == 0) mbar_expect_tx(BAR(bKFull0 + st), bytes);
+        if (gt >= nst && !(ok = wait(empty0 + st, gt / nst - 1))) break;
+        if (lane == 0) mbar_expect_tx(BAR(full0 + st), bytes);
         __syncwarp();
         if (slot >= 0) {
-          const uint32_t kdst = base + Ly::kK + st * Ly::kTile + lane * R * 128;
+          const uint32_t dst = ring + st * Ly::kTile + lane * R * 128;
 #pragma unroll
           for (int hf = 0; hf < Ly::kHalves; ++hf)
-            tma_load_3d(kdst + hf * Ly::kHalf, &tm_k, hf * 64, I.hk, slot, BAR(bKFull0 + st));
+            tma_load_3d(dst + hf * Ly::kHalf, map, hf * 64, I.hk, slot, BAR(full0 + st));
         }
-        last_k = gt;
-        if (gt >= 2 && !(ok = wait(bVEmpty0 + st, (gt >> 1) - 1))) break;
-        if (lane == 0) mbar_expect_tx(BAR(bVFull0 + st), bytes);
-        __syncwarp();
-        if (slot >= 0) {
-          const uint32_t vdst = base + Ly::kV + st * Ly::kTile + lane * R * 128;
-#pragma unroll
-          for (int hf = 0; hf < Ly::kHalves; ++hf)
-            tma_load_3d(vdst + hf * Ly::kHalf, &tm_v, hf * 64, I.hk, slot, BAR(bVFull0 + st));
-        }
-        last_v = gt;
+        last = gt;
       }
     }
     // drain: every copy this warp issued has landed before the CTA exits
     if (lane == 0) {
-      for (int t = max(0, last_k - 1); t <= last_k; ++t)
-        mbar_wait(BAR(bKFull0 + (t & 1)), (t >> 1) & 1, kWaitNs);
-      for (int t = max(0, last_v - 1); t <= last_v; ++t)
-        mbar_wait(BAR(bVFull0 + (t & 1)), (t >> 1) & 1, kWaitNs);
-      if (it > 0) mbar_wait(BAR(bQFull), (it - 1) & 1, kWaitNs);
+      for (int t = max(0, last - nst + 1); t <= last; ++t)
+        mbar_wait(BAR(full0 + t % nst), (t / nst) & 1, kWaitNs);
+      if (is_k && it > 0) mbar_wait(BAR(bQFull), (it - 1) & 1, kWaitNs);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -272,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdO = idesc_bf16(kM, D, true);
     auto issue_s = [&](int side, int g) {
       const uint32_t q0 = base + (side ? Ly::kQB : Ly::kQA);
-      const uint32_t k0 = base + Ly::kK + (g & 1) * Ly::kTile;
+      const uint32_t k0 = base + Ly::kK + (g % Ly::kKStages) * Ly::kTile;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * Ly::kHalf + (kk & 3) * 32;
@@ -282,15 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(BAR(side ? bSB : bSA));
     };
     auto issue_pv = [&](int side, int g, bool acc) {
-      const uint32_t p0 = base + Ly::kP;
-      const uint32_t v0 = base + Ly::kV + (g & 1) * Ly::kTile;
+      const uint32_t v0 = base + Ly::kV + (g % Ly::kVStages) * Ly::kTile;
 #pragma unroll
-      for (int kk = 0; kk < kN / 16; ++kk) {
-        const uint32_t aoff = (kk >> 2) * Ly::kHalf + (kk & 3) * 32;
-        mma_f16_ss(tmem + 256 + side * 128, smem_desc_sw128(p0 + aoff, 16, 1024),
+      for (int kk = 0; kk < kN / 16; ++kk)
+        mma_f16_ts(tmem + 256 + side * 128, tmem + side * 128 + kk * 8,
                    smem_desc_sw128(v0 + kk * 2048, Ly::kHalf, 1024), kIdO,
                    (acc || kk > 0) ? 1u : 0u);
-      }
       mma_commit(BAR(side ? bPvB : bPvA));
     };
     int gt = 0, it = 0, gB = 0, itB = 0;
@@ -302,23 +305,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool bad;
       if (!decode_item(a, e, pairs, I, bad)) continue;
       const bool hasB = I.h[1] >= 0;
-      if (!(ok = wait(bQFull, it) && wait(bKFull0 + (gt & 1), gt >> 1))) break;
+      if (!(ok = wait(bQFull, it) && wait(bKFull0 + gt % Ly::kKStages, gt / Ly::kKStages))) break;
       tc_fence_after();
       if (lane == 0) {
         issue_s(0, gt);
         if (hasB) issue_s(1, gt);
-        mma_commit(BAR(bKEmpty0 + (gt & 1)));
+        mma_commit(BAR(bKEmpty0 + gt % Ly::kKStages));
+        if (I.n == 1) mma_commit(BAR(bQFree));
       }
       __syncwarp();
       for (int j = 0; j < I.n; ++j) {
         const int g = gt + j;
+        const bool more = j + 1 < I.n;
         ok = wait(bPA, g) && (j > 0 || it == 0 || wait(bOFreeA, it - 1)) &&
-             wait(bVFull0 + (g & 1), g >> 1);
+             wait(bVFull0 + g % Ly::kVStages, g / Ly::kVStages);
         if (!ok) break;
         tc_fence_after();
         const int live = I.kv_end - j * kN;  // rows [live, 128) of V_j are not keys
         if (live < kN) {
-          uint8_t* vt = sgen + Ly::kV + (g & 1) * Ly::kTile;
+          uint8_t* vt = sgen + Ly::kV + (g % Ly::kVStages) * Ly::kTile;
           const int chunks = (kN - live) * 128 / 16;
           for (int hf = 0; hf < Ly::kHalves; ++hf) {
             uint4* p = reinterpret_cast<uint4*>(vt + hf * Ly::kHalf + live * 128);
@@ -329,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) issue_pv(0, g, j > 0);
         __syncwarp();
-        if (j + 1 < I.n) {
-          if (!(ok = wait(bKFull0 + ((g + 1) & 1), (g + 1) >> 1))) break;
+        if (more) {
+          if (!(ok = wait(bKFull0 + (g + 1) % Ly::kKStages, (g + 1) / Ly::kKStages))) break;
           tc_fence_after();
           if (lane == 0) issue_s(0, g + 1);
           __syncwarp();
@@ -340,19 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (lane == 0) {
             issue_pv(1, g, j > 0);
-            if (j + 1 < I.n) issue_s(1, g + 1);
+            if (more) issue_s(1, g + 1);
           }
           __syncwarp();
         }
         if (lane == 0) {
-          mma_commit(BAR(bVEmpty0 + (g & 1)));
-          if (j + 1 < I.n) mma_commit(BAR(bKEmpty0 + ((g + 1) & 1)));
+          mma_commit(BAR(bVEmpty0 + g % Ly::kVStages));
+          if (more) mma_commit(BAR(bKEmpty0 + (g + 1) % Ly::kKStages));
+          if (j + 2 == I.n) mma_commit(BAR(bQFree));  // the item's last S products are issued
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(BAR(bQFree));
-      __syncwarp();
       gt += I.n;
       ++it;
       if (hasB) {
@@ -371,9 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + side * 128 + lane_off;
     const uint32_t tO = tmem + 256 + side * 128 + lane_off;
-    const uint32_t prow = base + Ly::kP + r * 128;
-    int gt = 0, gx = 0, nB = 0;  // all tiles, this side's tiles, B tiles so far
-    bool prev_hasB = false;
+    int gx = 0;  // tiles this side has processed
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int e = slot_of(k, cta, G);
@@ -381,18 +383,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item I;
       bool bad;
       if (!decode_item(a, e, pairs, I, bad)) continue;
-      const bool hasB = I.h[1] >= 0;
-      if (side == 1 && !hasB) {
-        gt += I.n;
-        prev_hasB = false;
-        continue;
-      }
+      if (side == 1 && I.h[1] < 0) continue;
       const int i = I.i0 + r;
       const bool row_ok = i < I.qn;
       const int lim = I.c + i;  // last key position this row sees
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < I.n; ++j) {
-        const int g = gt + j;
+        // S_j ready; its commit also covers this side's earlier products, so
+        // the P columns and O may be rewritten below.
         if (!(ok = wait(side ? bSB : bSA, gx + j))) break;
         tc_fence_after();
         const int key0 = j * kN;
@@ -405,8 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int x = 0; x < 8; ++x) mx[x] = -INFINITY;
         if (full) {
-          // every key of the tile is visible: scores stay raw, the scale is
-          // folded into the exponent below (max commutes with a positive scale)
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
@@ -445,20 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           sm[(e2 + 1) & 7] += p1;
           flat[e2 >> 1] = pack_bf16(p0, p1);
         }
-        const uint32_t* pk = flat;
         l = l * alpha + (((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7])));
-        // the shared P buffer and this side's O must be free: wait for the
-        // last product issued before ours
-        if (side == 0) {
-          if (g > 0) {
-            if (prev_hasB) ok = wait(bPvB, nB - 1);
-            else ok = wait(bPvA, g - 1);
-          }
-        } else {
-          ok = wait(bPvA, g);
-        }
-        if (!ok) break;
-        tc_fence_after();
+        tmem_st32(tS, sr[0]);
+        tmem_st32(tS + 32, sr[1]);
         const bool need = j > 0 && m_new != m_used;
         if (__any_sync(0xffffffffu, need)) {
           const float f = need ? alpha : 1.f;
@@ -471,30 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e2 = 0; e2 < 32; ++e2) o[e2] = __float_as_uint(__uint_as_float(o[e2]) * f);
             tmem_st32(tO + cc * 32, o);
           }
-          tmem_wait_st();
         }
         m_used = m_new;
-        // P row -> smem, K-major with the 128-byte swizzle: 16-byte chunk q of
-        // row r in a 64-key half lands at chunk q ^ (r & 7).
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int q8 = 0; q8 < 8; ++q8) {
-            const uint32_t* w = &pk[hf * 32 + q8 * 4];  // keys hf*64 + q8*8 .. +7
-            const uint32_t addr = prow + hf * Ly::kHalf + ((q8 ^ (r & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(w[0]),
-                         "r"(w[1]), "r"(w[2]), "r"(w[3])
-                         : "memory");
-          }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(BAR(side ? bPB : bPA));
-        prev_hasB = hasB;
-        if (hasB) ++nB;
       }
       if (!ok) break;
       // epilogue: wait for this side's last product, normalise, store
-      if (!(ok = side == 0 ? wait(bPvA, gt + I.n - 1) : wait(bPvB, nB - 1))) break;
+      if (!(ok = wait(side ? bPvB : bPvA, gx + I.n - 1))) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
@@ -520,7 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(BAR(side ? bOFreeB : bOFreeA));
-      gt += I.n;
       gx += I.n;
     }
   }
