@@ -17,12 +17,13 @@
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3   softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
 //   warps 4-7   softmax + epilogue of tile B
-//   warp 8      TMA producer of Q_A/Q_B (per item) and K_j (3-stage ring)
+//   warp 8      TMA producer of Q_A/Q_B (per item) and the even blocks of K_j
 //   warp 9      TMEM allocation and MMA issue (one lane)
 //   warp 10     TMA producer of V_j (2-stage ring)
-//   warp 11     idle (completes the third warpgroup)
-// The producers' 32 lanes resolve a tile's blocks through the block table and
-// issue one TMA box each, in parallel.
+//   warp 11     TMA producer of the odd blocks of K_j (3-stage ring)
+// The producers' lanes resolve a tile's blocks through the block table and
+// issue one TMA box each; TMA issue is serialised within a warp, so spreading
+// the boxes of a tile over warps shortens it.
 // The softmax warpgroups raise their register limit to 200 and the third
 // warpgroup lowers its to 96 (256*200 + 128*96 = 63488 <= 384*168 launched;
 // per SM sub-partition 200+200+96 registers x 32 lanes <= 16384), so a softmax
@@ -72,6 +73,7 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kVWarp = 10;
+constexpr int kK2Warp = 11;
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -174,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       const bool many = i == bPA || i == bPB || i == bOFreeA || i == bOFreeB;
-      mbar_init(BAR(i), many ? 128u : 1u);
+      const bool kfull = i == bKFull0 || i == bKFull1 || i == bKFull2;  // two K producers
+      mbar_init(BAR(i), many ? 128u : (kfull ? 2u : 1u));
     }
     *abort_flag = 0u;
     fence_barrier_init();
@@ -201,10 +204,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp >= kProducerWarp) regs_decrease<96>();
-  if (warp == kProducerWarp || warp == kVWarp) {
+  if (warp == kProducerWarp || warp == kVWarp || warp == kK2Warp) {
     // ------------------------------------------------------------ producers
-    // warp 8: Q per item and the K tiles; warp 10: the V tiles.
-    const bool is_k = warp == kProducerWarp;
+    // warp 8: Q per item and K boxes 0, 2, 4, ...; warp 11: K boxes 1, 3, 5, ...;
+    // warp 10: every V box.
+    const bool is_k = warp != kVWarp;
+    const bool is_q = warp == kProducerWarp;
+    const int bstep = is_k ? 2 : 1;                  // box b = lane * bstep + boff
+    const int boff = warp == kK2Warp ? 1 : 0;
     const int nst = is_k ? Ly::kKStages : Ly::kVStages;
     const int full0 = is_k ? bKFull0 : bVFull0;
     const int empty0 = is_k ? bKEmpty0 : bVEmpty0;
@@ -220,10 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item I;
       bool bad;
       if (!decode_item(a, e, pairs, I, bad)) {
-        if (bad && is_k && lane == 0) flag_error(a.err, PA_DEV_BAD_LEN);
+        if (bad && is_q && lane == 0) flag_error(a.err, PA_DEV_BAD_LEN);
         continue;
       }
-      if (is_k) {
+      if (is_q) {
         if (it > 0 && !(ok = wait(bQFree, it - 1))) break;
         if (lane == 0) {
           const bool hasB = I.h[1] >= 0;
@@ -245,11 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int p0 = j * kN;
         const int nbox = (min(I.kv_end, p0 + kN) - p0 + R - 1) / R;
         int slot = -1;
-        if (lane < nbox) {
-          const int pos = p0 + lane * R;
+        const int b = lane * bstep + boff;
+        if (b < nbox) {
+          const int pos = p0 + b * R;
           const int pb = __ldg(bt + (pos >> a.bs_log2));
           if (pb >= 0 && pb < a.num_blocks) slot = (pb << a.bs_log2) + (pos & (bs - 1));
-          else if (is_k) flag_error(a.err, PA_DEV_BAD_BLOCK);
+          else flag_error(a.err, PA_DEV_BAD_BLOCK);
         }
         const uint32_t valid = __ballot_sync(0xffffffffu, slot >= 0);
         const uint32_t bytes = static_cast<uint32_t>(__popc(valid) * R * 128 * Ly::kHalves);
@@ -257,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_expect_tx(BAR(full0 + st), bytes);
         __syncwarp();
         if (slot >= 0) {
-          const uint32_t dst = ring + st * Ly::kTile + lane * R * 128;
+          const uint32_t dst = ring + st * Ly::kTile + b * R * 128;
 #pragma unroll
           for (int hf = 0; hf < Ly::kHalves; ++hf)
             tma_load_3d(dst + hf * Ly::kHalf, map, hf * 64, I.hk, slot, BAR(full0 + st));
@@ -269,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int t = max(0, last - nst + 1); t <= last; ++t)
         mbar_wait(BAR(full0 + t % nst), (t / nst) & 1, kWaitNs);
-      if (is_k && it > 0) mbar_wait(BAR(bQFull), (it - 1) & 1, kWaitNs);
+      if (is_q && it > 0) mbar_wait(BAR(bQFull), (it - 1) & 1, kWaitNs);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
