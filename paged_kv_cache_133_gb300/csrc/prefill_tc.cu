@@ -10,9 +10,13 @@
 //
 // Work item: 128 query tokens of one sequence for TWO query heads A and B of
 // the same kv head (so every K/V tile feeds both), or one head when the group
-// has an odd head left over.  The grid is persistent (one CTA per SM); CTAs
-// walk the item list in a boustrophedon order over "tile counted from the
-// end of its sequence", so the longest key ranges start first.
+// has an odd head left over.  An item's cost is its number of 128-key tiles;
+// token tile t of a sequence with c cached tokens has cost ceil(c/128) + t + 1
+// (one less for a short last tile).  Slots enumerate items by that level,
+// highest first, so the list is sorted by cost; the grid is persistent (one
+// CTA per SM) and CTAs take slots in boustrophedon rounds (k-th round: CTA i
+// takes k*G + i, or k*G + G-1-i when k is odd), which balances the per-CTA
+// cost to within a few tiles of the mean.
 //
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3   softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
@@ -105,11 +109,11 @@ struct Item {
   int s, hk, h[2], t0, qn, c, i0, kv_end, n;  // h[1] < 0: no second tile
 };
 
-// Work slot e -> item.  Slots enumerate (tile counted from the end, sequence,
-// kv head, head unit); a head unit is the 2*CL query heads one cluster of CL
-// CTAs serves (two per CTA); a slot whose tile does not exist is empty.
-template <int CL>
-__device__ bool decode_item(const AttnArgs& a, int e, int pairs, int rank, Item& it, bool& bad) {
+// Work slot e -> item.  Slots enumerate (cost level from max_level down to 1,
+// sequence, kv head, head pair); the sequence's tile at that level is
+// t = level - 1 - ceil(c / 128); a slot whose tile does not exist is empty.
+__device__ bool decode_item(const AttnArgs& a, int e, int pairs, int max_level, Item& it,
+                            bool& bad) {
   const int S_pre = a.num_seqs - a.num_decode;
   const int per_seq = a.hkv * pairs;
   const int per_z = per_seq * S_pre;
@@ -130,13 +134,13 @@ __device__ bool decode_item(const AttnArgs& a, int e, int pairs, int rank, Item&
     bad = true;
     return false;
   }
-  const int tile = (qn + kM - 1) / kM - 1 - z;
-  if (tile < 0) return false;
+  const int level = max_level - z;
+  const int tile = level - 1 - (L - qn + kN - 1) / kN;
+  if (tile < 0 || tile >= (qn + kM - 1) / kM) return false;
   it.s = s;
   it.hk = hk;
-  const int h0 = (p * CL + rank) * 2;  // first head of this CTA within the group
-  it.h[0] = hk * a.group + h0;
-  it.h[1] = h0 + 1 < a.group ? it.h[0] + 1 : -1;
+  it.h[0] = hk * a.group + 2 * p;
+  it.h[1] = 2 * p + 1 < a.group ? it.h[0] + 1 : -1;
   it.t0 = t0;
   it.qn = qn;
   it.c = L - qn;
@@ -151,22 +155,20 @@ __device__ __forceinline__ int slot_of(int k, int cta, int G) {
   return k * G + ((k & 1) ? (G - 1 - cta) : cta);
 }
 
-template <int D, int CL>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
-                      int total_slots) {
+                      int total_slots, int max_level) {
   using Ly = PpLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pairs = (a.group + 2 * CL - 1) / (2 * CL);  // head units per kv head
-  const int G = gridDim.x / CL, cta = blockIdx.x / CL;  // clusters walk the slots
-  const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const uint16_t all_ctas = static_cast<uint16_t>((1u << CL) - 1u);
+  const int pairs = (a.group + 1) >> 1;
+  const int G = gridDim.x, cta = blockIdx.x;
 
   const uint32_t bar0 = base + Ly::kBar;
   const uint32_t tmem_slot = bar0 + 8 * kNumBars;
@@ -182,9 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) {
       const bool many = i == bPA || i == bPB || i == bOFreeA || i == bOFreeB;
       const bool kfull = i == bKFull0 || i == bKFull1 || i == bKFull2;  // two K producers
-      const bool kvempty = i == bKEmpty0 || i == bKEmpty1 || i == bKEmpty2 || i == bVEmpty0 ||
-                           i == bVEmpty1;  // released by the MMA lane of every CTA of the cluster
-      mbar_init(BAR(i), many ? 128u : (kfull ? 2u : (kvempty ? static_cast<uint32_t>(CL) : 1u)));
+      mbar_init(BAR(i), many ? 128u : (kfull ? 2u : 1u));
     }
     *abort_flag = 0u;
     fence_barrier_init();
@@ -195,8 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_v);
   }
   tc_fence_before();
-  if (CL > 1) cluster_sync();  // every CTA's barriers exist before any multicast lands
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + Ly::kBar + 8 * kNumBars);
 
@@ -216,12 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producers
     // warp 8: Q per item and K boxes 0, 2, 4, ...; warp 11: K boxes 1, 3, 5, ...;
     // warp 10: every V box.
-    // With CL > 1 the CTAs of a cluster split every tile's boxes (box b is
-    // issued by rank b % CL) and multicast them to all CTAs; each warp still
-    // accounts for the bytes of its whole share, whoever issues them.
     const bool is_k = warp != kVWarp;
     const bool is_q = warp == kProducerWarp;
-    const int kw = warp == kK2Warp ? 1 : 0;
+    const int bstep = is_k ? 2 : 1;                  // box b = lane * bstep + boff
+    const int boff = warp == kK2Warp ? 1 : 0;
     const int nst = is_k ? Ly::kKStages : Ly::kVStages;
     const int full0 = is_k ? bKFull0 : bVFull0;
     const int empty0 = is_k ? bKEmpty0 : bVEmpty0;
@@ -236,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (e >= total_slots) break;
       Item I;
       bool bad;
-      if (!decode_item<CL>(a, e, pairs, rank, I, bad)) {
+      if (!decode_item(a, e, pairs, max_level, I, bad)) {
         if (bad && is_q && lane == 0) flag_error(a.err, PA_DEV_BAD_LEN);
         continue;
       }
@@ -262,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int p0 = j * kN;
         const int nbox = (min(I.kv_end, p0 + kN) - p0 + R - 1) / R;
         int slot = -1;
-        const int b = is_k ? ((lane / CL) * 2 + kw) * CL + lane % CL : lane;
+        const int b = lane * bstep + boff;
         if (b < nbox) {
           const int pos = p0 + b * R;
           const int pb = __ldg(bt + (pos >> a.bs_log2));
@@ -274,16 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (gt >= nst && !(ok = wait(empty0 + st, gt / nst - 1))) break;
         if (lane == 0) mbar_expect_tx(BAR(full0 + st), bytes);
         __syncwarp();
-        if (slot >= 0 && b % CL == rank) {
+        if (slot >= 0) {
           const uint32_t dst = ring + st * Ly::kTile + b * R * 128;
 #pragma unroll
-          for (int hf = 0; hf < Ly::kHalves; ++hf) {
-            if (CL > 1)
-              tma_load_3d_mc(dst + hf * Ly::kHalf, map, hf * 64, I.hk, slot, BAR(full0 + st),
-                             all_ctas);
-            else
-              tma_load_3d(dst + hf * Ly::kHalf, map, hf * 64, I.hk, slot, BAR(full0 + st));
-          }
+          for (int hf = 0; hf < Ly::kHalves; ++hf)
+            tma_load_3d(dst + hf * Ly::kHalf, map, hf * 64, I.hk, slot, BAR(full0 + st));
         }
         last = gt;
       }
@@ -319,11 +311,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (acc || kk > 0) ? 1u : 0u);
       mma_commit(BAR(side ? bPvB : bPvA));
     };
-    // a K or V stage is free again once every CTA of the cluster has read it
-    auto release = [&](int b) {
-      if (CL > 1) mma_commit_mc(BAR(b), all_ctas);
-      else mma_commit(BAR(b));
-    };
     int gt = 0, it = 0, gB = 0, itB = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -331,14 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (e >= total_slots) break;
       Item I;
       bool bad;
-      if (!decode_item<CL>(a, e, pairs, rank, I, bad)) continue;
+      if (!decode_item(a, e, pairs, max_level, I, bad)) continue;
       const bool hasB = I.h[1] >= 0;
       if (!(ok = wait(bQFull, it) && wait(bKFull0 + gt % Ly::kKStages, gt / Ly::kKStages))) break;
       tc_fence_after();
       if (lane == 0) {
         issue_s(0, gt);
         if (hasB) issue_s(1, gt);
-        release(bKEmpty0 + gt % Ly::kKStages);
+        mma_commit(BAR(bKEmpty0 + gt % Ly::kKStages));
         if (I.n == 1) mma_commit(BAR(bQFree));
       }
       __syncwarp();
@@ -378,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         if (lane == 0) {
-          release(bVEmpty0 + g % Ly::kVStages);
-          if (more) release(bKEmpty0 + (g + 1) % Ly::kKStages);
+          mma_commit(BAR(bVEmpty0 + g % Ly::kVStages));
+          if (more) mma_commit(BAR(bKEmpty0 + (g + 1) % Ly::kKStages));
           if (j + 2 == I.n) mma_commit(BAR(bQFree));  // the item's last S products are issued
         }
         __syncwarp();
@@ -410,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (e >= total_slots) break;
       Item I;
       bool bad;
-      if (!decode_item<CL>(a, e, pairs, rank, I, bad)) continue;
+      if (!decode_item(a, e, pairs, max_level, I, bad)) continue;
       if (side == 1 && I.h[1] < 0) continue;
       const int i = I.i0 + r;
       const bool row_ok = i < I.qn;
@@ -523,8 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 #undef BAR
   tc_fence_before();
-  if (CL > 1) cluster_sync();  // no CTA leaves while a peer may still signal or write into it
-  else __syncthreads();
+  __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -580,78 +566,36 @@ bool encode_cache(CUtensorMap* m, const void* ptr, const AttnArgs& a) {
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int cluster_size_for(const AttnArgs& a) {
-  const char* env = getenv("PA_PREFILL_CLUSTER");
-  if (env && strcmp(env, "0") == 0) return 1;
-  return a.group % 4 == 0 ? 2 : 1;
-}
+// Highest cost level: every visible key range is at most max_seq_len keys.
+int max_level_of(const AttnArgs& a) { return (a.max_seq_len + kN - 1) / kN + 1; }
 
-int64_t total_slots_of(const AttnArgs& a, int cl) {
-  const int64_t units = (a.group + 2 * cl - 1) / (2 * cl);
-  const int64_t tiles = (static_cast<int64_t>(a.max_query_len) + kM - 1) / kM;
-  return static_cast<int64_t>(a.hkv) * units * (a.num_seqs - a.num_decode) * tiles;
-}
-
-template <int D, int CL>
-cudaError_t launch_tc_dc(const AttnArgs& a, cudaStream_t st, const CUtensorMap& mq,
-                         const CUtensorMap& mk, const CUtensorMap& mv) {
-  using Ly = PpLayout<D>;
-  static int max_clusters[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_clusters[dev] == 0) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
-    if (e != cudaSuccess) return e;
-    int n = device_num_sms() / CL;
-    if (CL > 1) {
-      cudaLaunchConfig_t probe = {};
-      probe.gridDim = dim3(CL * n);
-      probe.blockDim = dim3(kThreads);
-      probe.dynamicSmemBytes = Ly::kAlloc;
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = CL;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      probe.attrs = at;
-      probe.numAttrs = 1;
-      int m = 0;
-      if (cudaOccupancyMaxActiveClusters(&m, prefill_tc_kernel<D, CL>, &probe) == cudaSuccess &&
-          m > 0 && m < n)
-        n = m;
-      cudaGetLastError();
-    }
-    max_clusters[dev] = n > 0 ? n : 1;
-  }
-  const int64_t total = total_slots_of(a, CL);
-  const int clusters = static_cast<int>(total < max_clusters[dev] ? total : max_clusters[dev]);
-  if (clusters <= 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters * CL);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Ly::kAlloc;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = CL;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  count_launch();
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL>, mq, mk, mv, a,
-                            static_cast<int>(total));
+int64_t total_slots_of(const AttnArgs& a) {
+  const int64_t pairs = (a.group + 1) / 2;
+  return static_cast<int64_t>(a.hkv) * pairs * (a.num_seqs - a.num_decode) * max_level_of(a);
 }
 
 template <int D>
 cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
+  using Ly = PpLayout<D>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
   CUtensorMap mq, mk, mv;
   if (!encode_q(&mq, a) || !encode_cache(&mk, a.k_cache, a) || !encode_cache(&mv, a.v_cache, a))
     return cudaErrorNotSupported;  // nothing launched: the caller takes the general kernel
-  return cluster_size_for(a) == 2 ? launch_tc_dc<D, 2>(a, st, mq, mk, mv)
-                                  : launch_tc_dc<D, 1>(a, st, mq, mk, mv);
+  const int total = static_cast<int>(total_slots_of(a));
+  const int sms = device_num_sms();
+  const int grid = total < sms ? total : sms;
+  if (grid <= 0) return cudaSuccess;
+  count_launch();
+  prefill_tc_kernel<D><<<grid, kThreads, Ly::kAlloc, st>>>(mq, mk, mv, a, total, max_level_of(a));
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -665,7 +609,7 @@ bool prefill_tc_supported(const AttnArgs& a) {
   if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k_cache) |
        reinterpret_cast<uintptr_t>(a.v_cache)) & 15u)
     return false;
-  if (total_slots_of(a, 1) > INT_MAX / 2) return false;
+  if (total_slots_of(a) > INT_MAX / 2) return false;
   return encode_fn() != nullptr;
 }
 
