@@ -83,10 +83,12 @@ int pa_write_kv(const void* k, const void* v, int64_t k_stride_t, int64_t v_stri
                 uint32_t* err_flag, void* stream);
 
 /*
- * pa_attention_workspace_size — bytes of scratch pa_attention needs for the
- * split-KV decode partials (fp32 running max, sum and weighted value per
- * split, sequence and query head).  Depends on the current device's SM count;
- * query it on the device that will run the call.  0 means no workspace.
+ * pa_attention_workspace_size — bytes of scratch pa_attention needs: a
+ * 256-byte header (the prefill kernel's work-queue counter, zeroed by each
+ * call) followed by the split-KV decode partials (fp32 running max, sum and
+ * weighted value per split, sequence and query head) when the decode rows are
+ * split.  Never 0.  Depends on the current device's SM count; query it on the
+ * device that will run the call.
  */
 size_t pa_attention_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv_heads,
                                    int head_dim, int max_seq_len);
@@ -110,7 +112,9 @@ size_t pa_attention_workspace_size(int num_decode_seqs, int num_q_heads, int num
  *                   (like max_seqlen_q / max_seqlen_k of "vLLM 原理" §3.7).
  *   scale    softmax scale (1/sqrt(head_dim) in the usual case).
  *   workspace, workspace_bytes  device scratch of at least
- *                   pa_attention_workspace_size(num_decode_seqs, ...) bytes.
+ *                   pa_attention_workspace_size(num_decode_seqs, ...) bytes,
+ *                   16-byte aligned; its contents need no initialisation.
+ *                   Calls that overlap on the GPU must not share it.
  * out[t, h] = sum_p softmax_p(scale * q[t,h] . k_p) v_p over the visible keys
  * of t's sequence, accumulated in fp32, rounded once to bf16.
  * Supports head_dim 64 or 128, block_size a power of two in [1, 256],

@@ -41,6 +41,8 @@ static int ilog2_exact(int x) {
   return l;
 }
 
+// Workspace = kWorkspaceHeader bytes (prefill work-queue counter) followed by
+// the split-KV decode partials, when the decode rows are split.
 static size_t decode_workspace(int num_decode, int hq, int hkv, int head_dim, int max_seq_len,
                                int* part, int* nsplit) {
   *part = 64;
@@ -113,8 +115,8 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
 size_t pa_attention_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv_heads,
                                    int head_dim, int max_seq_len) {
   int part, nsplit;
-  return decode_workspace(num_decode_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
-                          &part, &nsplit);
+  return kWorkspaceHeader + decode_workspace(num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             max_seq_len, &part, &nsplit);
 }
 
 int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
@@ -174,15 +176,19 @@ int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_strid
   a.err = err_flag;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t decode_need = num_decode_seqs > 0 && max_seq_len > 0
+                                 ? decode_workspace(num_decode_seqs, num_q_heads, num_kv_heads,
+                                                    head_dim, max_seq_len, &a.part, &a.nsplit)
+                                 : 0;
+  if (!workspace || workspace_bytes < kWorkspaceHeader + decode_need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 15u))
+    return PA_ERR_WORKSPACE;
+  a.sched = static_cast<unsigned int*>(workspace);
+  if (decode_need > 0) {
+    a.ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader);
+    a.ws_ml = a.ws_o + static_cast<size_t>(a.nsplit) * num_decode_seqs * num_q_heads * head_dim;
+  }
   if (num_decode_seqs > 0 && max_seq_len > 0) {
-    const size_t need = decode_workspace(num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
-                                         max_seq_len, &a.part, &a.nsplit);
-    if (need > 0) {
-      if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
-        return PA_ERR_WORKSPACE;
-      a.ws_o = static_cast<float*>(workspace);
-      a.ws_ml = a.ws_o + static_cast<size_t>(a.nsplit) * num_decode_seqs * num_q_heads * head_dim;
-    }
     int rc = cuda_status(launch_decode(a, st));
     if (rc != PA_OK) return rc;
   }

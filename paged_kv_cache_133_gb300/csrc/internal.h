@@ -39,7 +39,12 @@ struct AttnArgs {
   int nsplit;    // grid splits = ceil(max_seq_len / part)
   float* ws_o;   // [nsplit, num_decode, hq, head_dim]
   float* ws_ml;  // [nsplit, num_decode, hq, 2]
+  // prefill work queue: a counter in the workspace header, zeroed per call
+  unsigned int* sched;
 };
+
+// Bytes at the start of the workspace reserved for the prefill work queue.
+constexpr size_t kWorkspaceHeader = 256;
 
 // Split-KV partition for the decode rows; shared by the workspace query and the
 // launch so that both agree.

@@ -13,21 +13,21 @@
 // has an odd head left over.  An item's cost is its number of 128-key tiles;
 // token tile t of a sequence with c cached tokens has cost ceil(c/128) + t + 1
 // (one less for a short last tile).  Slots enumerate items by that level,
-// highest first, so the list is sorted by cost; the grid is persistent (one
-// CTA per SM) and CTAs take slots in boustrophedon rounds (k-th round: CTA i
-// takes k*G + i, or k*G + G-1-i when k is odd), which balances the per-CTA
-// cost to within a few tiles of the mean.
+// highest first, so the list is sorted by cost.  The grid is persistent (one
+// CTA per SM); a scheduler warp in each CTA takes the next slot from a global
+// counter (atomicAdd) whenever its CTA has room, so CTAs that drew cheap
+// items draw more and all finish together.
 //
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3   softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
 //   warps 4-7   softmax + epilogue of tile B
-//   warp 8      TMA producer of Q_A/Q_B (per item) and the even blocks of K_j
+//   warp 8      TMA producer of Q_A/Q_B (per item) and K_j (3-stage ring)
 //   warp 9      TMEM allocation and MMA issue (one lane)
 //   warp 10     TMA producer of V_j (2-stage ring)
-//   warp 11     TMA producer of the odd blocks of K_j (3-stage ring)
+//   warp 11     scheduler: draws items from the global queue and hands them to
+//               the other roles through a 2-entry shared-memory ring
 // The producers' lanes resolve a tile's blocks through the block table and
-// issue one TMA box each; TMA issue is serialised within a warp, so spreading
-// the boxes of a tile over warps shortens it.
+// issue one TMA box each.
 // The softmax warpgroups raise their register limit to 200 and the third
 // warpgroup lowers its to 96 (256*200 + 128*96 = 63488 <= 384*168 launched;
 // per SM sub-partition 200+200+96 registers x 32 lanes <= 16384), so a softmax
@@ -77,7 +77,7 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kVWarp = 10;
-constexpr int kK2Warp = 11;
+constexpr int kSchedWarp = 11;
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -94,7 +94,7 @@ struct PpLayout {
   static constexpr int kK = 2 * kTile;
   static constexpr int kV = kK + kKStages * kTile;
   static constexpr int kBar = kV + kVStages * kTile;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kBytes = kBar + 512;  // barriers, TMEM slot, flags, item ring
   static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1 KB
 };
 
@@ -102,8 +102,14 @@ enum : int {
   bQFull, bQFree,
   bKFull0, bKFull1, bKFull2, bKEmpty0, bKEmpty1, bKEmpty2,
   bVFull0, bVFull1, bVEmpty0, bVEmpty1,
-  bSA, bSB, bPA, bPB, bPvA, bPvB, bOFreeA, bOFreeB, bDrain, kNumBars
+  bSA, bSB, bPA, bPB, bPvA, bPvB, bOFreeA, bOFreeB, bDrain,
+  bItemFull0, bItemFull1, bItemEmpty0, bItemEmpty1, kNumBars
 };
+
+// Threads that take each item from the ring: one lane of the K producer, the
+// MMA and the V producer warps, and every softmax thread.
+constexpr uint32_t kItemReaders = 3 + 256;
+constexpr int kRingOffset = 8 * 32;  // bytes after the barriers (TMEM slot + flags first)
 
 struct Item {
   int s, hk, h[2], t0, qn, c, i0, kv_end, n;  // h[1] < 0: no second tile
@@ -150,11 +156,6 @@ __device__ bool decode_item(const AttnArgs& a, int e, int pairs, int max_level, 
   return true;
 }
 
-// Slot of the k-th item of CTA `cta` among G CTAs (boustrophedon rounds).
-__device__ __forceinline__ int slot_of(int k, int cta, int G) {
-  return k * G + ((k & 1) ? (G - 1 - cta) : cta);
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -168,12 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sgen = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pairs = (a.group + 1) >> 1;
-  const int G = gridDim.x, cta = blockIdx.x;
 
   const uint32_t bar0 = base + Ly::kBar;
   const uint32_t tmem_slot = bar0 + 8 * kNumBars;
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(sgen + Ly::kBar + 8 * kNumBars + 4);
+  Item* ring = reinterpret_cast<Item*>(sgen + Ly::kBar + kRingOffset);
 #define BAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
 
   if (warp == kMmaWarp) {
@@ -183,8 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       const bool many = i == bPA || i == bPB || i == bOFreeA || i == bOFreeB;
-      const bool kfull = i == bKFull0 || i == bKFull1 || i == bKFull2;  // two K producers
-      mbar_init(BAR(i), many ? 128u : (kfull ? 2u : 1u));
+      const bool readers = i == bItemEmpty0 || i == bItemEmpty1;
+      mbar_init(BAR(i), many ? 128u : (readers ? kItemReaders : 1u));
     }
     *abort_flag = 0u;
     fence_barrier_init();
@@ -210,33 +211,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     return false;
   };
 
+  // Take item number `it` from the ring (every thread of a reading role calls
+  // this; `arrive` is true for the thread that reports the entry consumed).
+  auto next_item = [&](int it, Item& I, bool arrive) -> bool {
+    const int slot = it & 1;
+    if (!wait(bItemFull0 + slot, it >> 1)) return false;
+    I = ring[slot];  // ordered after the acquiring wait (asm with a memory clobber)
+    if (arrive) mbar_arrive(BAR(bItemEmpty0 + slot));
+    return I.n > 0;
+  };
+
   if (warp >= kProducerWarp) regs_decrease<96>();
-  if (warp == kProducerWarp || warp == kVWarp || warp == kK2Warp) {
+  if (warp == kSchedWarp) {
+    // ------------------------------------------------------------ scheduler
+    if (lane == 0) {
+      for (int it = 0;; ++it) {
+        Item I;
+        I.n = 0;
+        while (true) {
+          const int e = static_cast<int>(atomicAdd(a.sched, 1u));
+          if (e >= total_slots) break;
+          bool bad;
+          if (decode_item(a, e, pairs, max_level, I, bad)) break;
+          if (bad) flag_error(a.err, PA_DEV_BAD_LEN);
+        }
+        const int slot = it & 1;
+        if (it >= 2 && !wait(bItemEmpty0 + slot, (it >> 1) - 1)) break;
+        ring[slot] = I;  // published by the releasing arrive below
+        mbar_arrive(BAR(bItemFull0 + slot));  // release: the entry is visible to waiters
+        if (I.n <= 0) break;
+      }
+    }
+    __syncwarp();
+  }
+  if (warp == kProducerWarp || warp == kVWarp) {
     // ------------------------------------------------------------ producers
-    // warp 8: Q per item and K boxes 0, 2, 4, ...; warp 11: K boxes 1, 3, 5, ...;
-    // warp 10: every V box.
-    const bool is_k = warp != kVWarp;
-    const bool is_q = warp == kProducerWarp;
-    const int bstep = is_k ? 2 : 1;                  // box b = lane * bstep + boff
-    const int boff = warp == kK2Warp ? 1 : 0;
+    // warp 8: Q per item and the K tiles; warp 10: the V tiles.
+    const bool is_k = warp == kProducerWarp;
+    const bool is_q = is_k;
     const int nst = is_k ? Ly::kKStages : Ly::kVStages;
     const int full0 = is_k ? bKFull0 : bVFull0;
     const int empty0 = is_k ? bKEmpty0 : bVEmpty0;
-    const uint32_t ring = base + (is_k ? Ly::kK : Ly::kV);
+    const uint32_t stage0 = base + (is_k ? Ly::kK : Ly::kV);
     const CUtensorMap* map = is_k ? &tm_k : &tm_v;
     const int bs = 1 << a.bs_log2;
     const int R = bs < kN ? bs : kN;  // cache rows per TMA box; lane b owns box b
     int gt = 0, it = 0, last = -1;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int e = slot_of(k, cta, G);
-      if (e >= total_slots) break;
       Item I;
-      bool bad;
-      if (!decode_item(a, e, pairs, max_level, I, bad)) {
-        if (bad && is_q && lane == 0) flag_error(a.err, PA_DEV_BAD_LEN);
-        continue;
-      }
+      if (!next_item(k, I, false)) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(bItemEmpty0 + (k & 1)));
       if (is_q) {
         if (it > 0 && !(ok = wait(bQFree, it - 1))) break;
         if (lane == 0) {
@@ -259,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int p0 = j * kN;
         const int nbox = (min(I.kv_end, p0 + kN) - p0 + R - 1) / R;
         int slot = -1;
-        const int b = lane * bstep + boff;
+        const int b = lane;
         if (b < nbox) {
           const int pos = p0 + b * R;
           const int pb = __ldg(bt + (pos >> a.bs_log2));
@@ -272,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_expect_tx(BAR(full0 + st), bytes);
         __syncwarp();
         if (slot >= 0) {
-          const uint32_t dst = ring + st * Ly::kTile + b * R * 128;
+          const uint32_t dst = stage0 + st * Ly::kTile + b * R * 128;
 #pragma unroll
           for (int hf = 0; hf < Ly::kHalves; ++hf)
             tma_load_3d(dst + hf * Ly::kHalf, map, hf * 64, I.hk, slot, BAR(full0 + st));
@@ -314,11 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int gt = 0, it = 0, gB = 0, itB = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int e = slot_of(k, cta, G);
-      if (e >= total_slots) break;
       Item I;
-      bool bad;
-      if (!decode_item(a, e, pairs, max_level, I, bad)) continue;
+      if (!next_item(k, I, false)) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(bItemEmpty0 + (k & 1)));
       const bool hasB = I.h[1] >= 0;
       if (!(ok = wait(bQFull, it) && wait(bKFull0 + gt % Ly::kKStages, gt / Ly::kKStages))) break;
       tc_fence_after();
@@ -393,11 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int gx = 0;  // tiles this side has processed
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int e = slot_of(k, cta, G);
-      if (e >= total_slots) break;
       Item I;
-      bool bad;
-      if (!decode_item(a, e, pairs, max_level, I, bad)) continue;
+      if (!next_item(k, I, true)) break;
       if (side == 1 && I.h[1] < 0) continue;
       const int i = I.i0 + r;
       const bool row_ok = i < I.qn;
@@ -593,6 +615,8 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   const int sms = device_num_sms();
   const int grid = total < sms ? total : sms;
   if (grid <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
   count_launch();
   prefill_tc_kernel<D><<<grid, kThreads, Ly::kAlloc, st>>>(mq, mk, mv, a, total, max_level_of(a));
   return cudaGetLastError();
