@@ -21,11 +21,12 @@
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3   softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
 //   warps 4-7   softmax + epilogue of tile B
-//   warp 8      TMA producer of Q_A/Q_B (per item) and K_j (3-stage ring)
+//   warp 8      TMA producer of K_j (3-stage ring)
 //   warp 9      TMEM allocation and MMA issue (one lane)
 //   warp 10     TMA producer of V_j (2-stage ring)
-//   warp 11     scheduler: draws items from the global queue and hands them to
-//               the other roles through a 2-entry shared-memory ring
+//   warp 11     scheduler: draws items from the global queue, hands them to the
+//               other roles through a 2-entry shared-memory ring, and loads
+//               each item's Q_A/Q_B once the previous item's last S is done
 // The producers' lanes resolve a tile's blocks through the block table and
 // issue one TMA box each.
 // The softmax warpgroups raise their register limit to 200 and the third
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kSchedWarp) {
     // ------------------------------------------------------------ scheduler
     if (lane == 0) {
+      int q_issued = 0;
       for (int it = 0;; ++it) {
         Item I;
         I.n = 0;
@@ -240,15 +242,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         ring[slot] = I;  // published by the releasing arrive below
         mbar_arrive(BAR(bItemFull0 + slot));  // release: the entry is visible to waiters
         if (I.n <= 0) break;
+        // Q of this item, into the Q buffers the previous item has finished with
+        if (it > 0 && !wait(bQFree, it - 1)) break;
+        const bool hasB = I.h[1] >= 0;
+        mbar_expect_tx(BAR(bQFull), Ly::kTile * (hasB ? 2 : 1));
+#pragma unroll
+        for (int hf = 0; hf < Ly::kHalves; ++hf) {
+          tma_load_2d(base + Ly::kQA + hf * Ly::kHalf, &tm_q, I.h[0] * D + hf * 64, I.t0 + I.i0,
+                      BAR(bQFull));
+          if (hasB)
+            tma_load_2d(base + Ly::kQB + hf * Ly::kHalf, &tm_q, I.h[1] * D + hf * 64,
+                        I.t0 + I.i0, BAR(bQFull));
+        }
+        q_issued = it + 1;
       }
+      // drain: the last Q copy has landed before the CTA exits
+      if (q_issued > 0) mbar_wait(BAR(bQFull), (q_issued - 1) & 1, kWaitNs);
     }
     __syncwarp();
   }
   if (warp == kProducerWarp || warp == kVWarp) {
     // ------------------------------------------------------------ producers
-    // warp 8: Q per item and the K tiles; warp 10: the V tiles.
+    // warp 8: the K tiles; warp 10: the V tiles.
     const bool is_k = warp == kProducerWarp;
-    const bool is_q = is_k;
     const int nst = is_k ? Ly::kKStages : Ly::kVStages;
     const int full0 = is_k ? bKFull0 : bVFull0;
     const int empty0 = is_k ? bKEmpty0 : bVEmpty0;
@@ -263,21 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!next_item(k, I, false)) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(bItemEmpty0 + (k & 1)));
-      if (is_q) {
-        if (it > 0 && !(ok = wait(bQFree, it - 1))) break;
-        if (lane == 0) {
-          const bool hasB = I.h[1] >= 0;
-          mbar_expect_tx(BAR(bQFull), Ly::kTile * (hasB ? 2 : 1));
-#pragma unroll
-          for (int hf = 0; hf < Ly::kHalves; ++hf) {
-            tma_load_2d(base + Ly::kQA + hf * Ly::kHalf, &tm_q, I.h[0] * D + hf * 64,
-                        I.t0 + I.i0, BAR(bQFull));
-            if (hasB)
-              tma_load_2d(base + Ly::kQB + hf * Ly::kHalf, &tm_q, I.h[1] * D + hf * 64,
-                          I.t0 + I.i0, BAR(bQFull));
-          }
-        }
-      }
       ++it;
       const int32_t* bt = a.block_tables + static_cast<int64_t>(I.s) * a.max_blocks;
       for (int j = 0; j < I.n; ++j, ++gt) {
@@ -310,7 +311,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int t = max(0, last - nst + 1); t <= last; ++t)
         mbar_wait(BAR(full0 + t % nst), (t / nst) & 1, kWaitNs);
-      if (is_q && it > 0) mbar_wait(BAR(bQFull), (it - 1) & 1, kWaitNs);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
