@@ -1,8 +1,10 @@
 // C ABI entry points: host-side validation, workspace sizing and dispatch.
 // Nothing here allocates device memory or synchronises with the device.
 #include <math.h>
+#include <stdlib.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "internal.h"
 #include "pa.h"
@@ -24,6 +26,42 @@ int device_num_sms() {
     n = 148;
   if (dev >= 0 && dev < 64) cache[dev] = n;
   return n;
+}
+
+// Per-device side stream and fork/join events for running the decode rows
+// concurrently with the persistent prefill kernel.  Created once per device;
+// no device memory.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ready = false;
+};
+static SideStream g_side[64];
+static std::mutex g_side_mu;
+
+static SideStream* side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream& s = g_side[dev];
+  if (!s.ready) {
+    if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    s.ready = true;
+  }
+  return &s;
+}
+
+// SMs given to the decode rows while the prefill kernel runs beside them:
+// PA_MIXED_DECODE_SMS overrides, else 40 % of the SMs.
+static int mixed_decode_sms(int num_sms) {
+  const char* env = getenv("PA_MIXED_DECODE_SMS");
+  if (env) {
+    const int v = atoi(env);
+    if (v <= 0) return 0;
+    return v < num_sms - 1 ? v : num_sms - 1;
+  }
+  return (num_sms * 2) / 5;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -188,11 +226,39 @@ int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_strid
     a.ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader);
     a.ws_ml = a.ws_o + static_cast<size_t>(a.nsplit) * num_decode_seqs * num_q_heads * head_dim;
   }
-  if (num_decode_seqs > 0 && max_seq_len > 0) {
+  const bool has_decode = num_decode_seqs > 0 && max_seq_len > 0;
+  const bool has_prefill = num_seqs > num_decode_seqs && max_query_len > 0;
+  // Mixed step: the decode rows are HBM-bound and the tensor-core prefill is
+  // bound by its own TMA stream, so they run side by side: the persistent
+  // prefill kernel takes all but mixed_decode_sms() SMs on the caller's
+  // stream and the decode launches on a side stream (fork/join with events,
+  // which CUDA graph capture also records).
+  const int reserve = has_decode && has_prefill && prefill_tc_supported(a)
+                          ? mixed_decode_sms(device_num_sms())
+                          : 0;
+  if (reserve > 0) {
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream* side = side_stream();
+    if (side) {
+      if (cudaEventRecord(side->fork, st) != cudaSuccess ||
+          cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+        return cuda_status(cudaGetLastError());
+      a.max_ctas = device_num_sms() - reserve;
+      int rc = cuda_status(launch_prefill(a, st));
+      if (rc != PA_OK) return rc;
+      rc = cuda_status(launch_decode(a, side->stream));
+      if (rc != PA_OK) return rc;
+      if (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
+          cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
+        return cuda_status(cudaGetLastError());
+      return PA_OK;
+    }
+  }
+  if (has_decode) {
     int rc = cuda_status(launch_decode(a, st));
     if (rc != PA_OK) return rc;
   }
-  if (num_seqs > num_decode_seqs && max_query_len > 0) {
+  if (has_prefill) {
     int rc = cuda_status(launch_prefill(a, st));
     if (rc != PA_OK) return rc;
   }

@@ -41,6 +41,8 @@ struct AttnArgs {
   float* ws_ml;  // [nsplit, num_decode, hq, 2]
   // prefill work queue: a counter in the workspace header, zeroed per call
   unsigned int* sched;
+  // cap on the persistent prefill grid (0: one CTA per SM)
+  int max_ctas;
 };
 
 // Bytes at the start of the workspace reserved for the prefill work queue.

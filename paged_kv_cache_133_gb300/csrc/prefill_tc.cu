@@ -612,7 +612,8 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   if (!encode_q(&mq, a) || !encode_cache(&mk, a.k_cache, a) || !encode_cache(&mv, a.v_cache, a))
     return cudaErrorNotSupported;  // nothing launched: the caller takes the general kernel
   const int total = static_cast<int>(total_slots_of(a));
-  const int sms = device_num_sms();
+  int sms = device_num_sms();
+  if (a.max_ctas > 0 && a.max_ctas < sms) sms = a.max_ctas;  // SMs left to a concurrent decode
   const int grid = total < sms ? total : sms;
   if (grid <= 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
