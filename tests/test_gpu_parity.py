@@ -279,3 +279,67 @@ def test_prefill_full_size_both_kernels_agree(cfg, monkeypatch):
     d = (out_tc.float() - out_mma.float()).abs()
     assert torch.isfinite(out_tc.float()).all()
     assert d.max().item() <= 2e-2 and d.mean().item() <= 2e-3
+
+
+def test_workspace_reused_across_calls():
+    # the prefill work queue lives in the workspace header and must restart
+    # from zero on every call, whatever the previous call left there
+    lay = _prefill_cases()[0]
+    ts = workloads.make_tensors(lay, seed=12, poison=True)
+    g = {k: v.to(DEV) for k, v in ts.items()}
+    md = H.device_meta(lay, DEV)
+    need = pa.workspace_size(lay.num_decode_seqs, lay.num_q_heads, lay.num_kv_heads,
+                             lay.head_dim, lay.max_seq_len)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)
+    out1 = H.run_step(lay, g, md, workspace=ws).clone()
+    out2 = H.run_step(lay, g, md, workspace=ws).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    H.assert_close(H.f64(out1), H.oracle_full(lay, ts), "reused workspace")
+
+
+def test_mixed_step_side_by_side_is_bitwise_identical(monkeypatch):
+    # decode rows beside the prefill kernel (default) or after it: same bits
+    lay = workloads.custom_layout("mix", [900, 40, 3000, 12, 0, 700], [1, 1, 1, 1, 300, 150], 16, 4,
+                                  128, 16, 600, 41)
+    ts = workloads.make_tensors(lay, seed=13, poison=True)
+    g = {k: v.to(DEV) for k, v in ts.items()}
+    md = H.device_meta(lay, DEV)
+    monkeypatch.delenv("PA_MIXED_DECODE_SMS", raising=False)
+    out1 = H.run_step(lay, g, md).clone()
+    monkeypatch.setenv("PA_MIXED_DECODE_SMS", "0")
+    out2 = H.run_step(lay, g, md).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    H.assert_close(H.f64(out1), H.oracle_full(lay, ts), "mixed")
+
+
+def test_step_replays_from_a_cuda_graph():
+    # every call is stream-ordered and allocation-free, so a whole step
+    # (copy-on-write copies, scatter, attention with decode beside prefill)
+    # can be captured once and replayed
+    lay = workloads.shared_prefix_layout(0, num_seqs=6, prompt=512, tail_max=40, num_q_heads=16,
+                                         num_kv_heads=4, num_blocks=256)
+    lay2 = workloads.custom_layout("gmix", [300, 60, 0], [1, 1, 200], 16, 4, 128, 16, 64, 7)
+    for L in (lay, lay2):
+        ts = workloads.make_tensors(L, seed=14, poison=True)
+        g = {k: v.to(DEV) for k, v in ts.items()}
+        md = H.device_meta(L, DEV)
+        need = pa.workspace_size(L.num_decode_seqs, L.num_q_heads, L.num_kv_heads, L.head_dim,
+                                 L.max_seq_len)
+        ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+        out = torch.empty_like(g["q"])
+        H.run_step(L, g, md, out=out, workspace=ws)          # first call: per-device set-up
+        torch.cuda.synchronize()
+        expect = out.clone()
+        out.zero_()
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                H.run_step(L, g, md, out=out, workspace=ws)
+        torch.cuda.current_stream().wait_stream(s)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), expect.view(torch.int16))
