@@ -403,6 +403,64 @@ def secondary(dev, steps, warmup, peaks):
                     "ms_per_step": ms, "ms_attention": attn_ms,
                     "additive_roofline_ms": t_star * 1e3, "frac": t_star * 1e3 / ms}
     del st
+    res["swap"] = swap_leg(dev)
+    return res
+
+
+def swap_leg(dev, iters=20, warmup=3, pairs=4096, seed=0):
+    """Block swap between the device pool and a pool in page-locked host memory.
+
+    ``pairs`` random blocks of the decode pool's shape (bs 16, 8 KV heads, D 128:
+    64 KiB of K+V per block) go device -> host, then host -> device into other
+    blocks.  The link's own ceiling is one contiguous DMA copy of the same bytes
+    (cudaMemcpyAsync through ``copy_``), timed the same way in each direction.
+    """
+    import torch
+    import paged_kv_cache_133_gb300 as pa
+    rng = np.random.default_rng(seed)
+    bs, hkv, d = 16, 8, 128
+    n_dev, n_host = 3 * pairs, 2 * pairs
+    shape = (bs, hkv, d)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    dk = torch.randn((n_dev,) + shape, generator=g, device=dev, dtype=torch.bfloat16)
+    dv = torch.randn((n_dev,) + shape, generator=g, device=dev, dtype=torch.bfloat16)
+    hk = torch.empty((n_host,) + shape, dtype=torch.bfloat16, pin_memory=True)
+    hv = torch.empty((n_host,) + shape, dtype=torch.bfloat16, pin_memory=True)
+    src = rng.permutation(n_dev)[:pairs]
+    host = rng.permutation(n_host)[:pairs]
+    back = rng.permutation(n_dev)[:pairs]
+    p_out = torch.from_numpy(np.stack([src, host], 1).astype(np.int32)).to(dev)
+    p_in = torch.from_numpy(np.stack([host, back], 1).astype(np.int32)).to(dev)
+    nbytes = 2 * pairs * bs * hkv * d * 2
+    st = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(iters):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / iters
+
+    ms_out = timed(lambda: pa.swap_blocks(dk, dv, hk, hv, p_out))
+    ms_in = timed(lambda: pa.swap_blocks(hk, hv, dk, dv, p_in))
+    flat_d = dk[:2 * pairs].view(-1)
+    flat_h = hk.view(-1)
+    ms_d2h = timed(lambda: flat_h.copy_(flat_d, non_blocking=True))
+    ms_h2d = timed(lambda: flat_d.copy_(flat_h, non_blocking=True))
+    gbs = lambda ms: nbytes / (ms * 1e-3) / 1e9
+    res = {"workload": f"{pairs} random blocks of 16 x 8 x 128 bf16 (K+V {nbytes >> 20} MiB) between HBM and pinned host memory",
+           "metric": "swap GB/s (K+V bytes moved)",
+           "swap_out": {"ms": ms_out, "GB/s": gbs(ms_out), "dma_contiguous_GB/s": gbs(ms_d2h),
+                        "frac_of_dma": ms_d2h / ms_out},
+           "swap_in": {"ms": ms_in, "GB/s": gbs(ms_in), "dma_contiguous_GB/s": gbs(ms_h2d),
+                       "frac_of_dma": ms_h2d / ms_in}}
+    del dk, dv, hk, hv
     return res
 
 

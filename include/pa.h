@@ -141,6 +141,33 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
                    uint32_t* err_flag, void* stream);
 
 /*
+ * pa_swap_blocks — move whole blocks between two K/V pools, e.g. a GPU pool
+ * and a pool in host memory, for CPU offload of the cache: "LLM 推理引擎
+ * Continuous Batching 与 PagedAttention：从 vLLM 原理到生产级部署实战" §4.4
+ * (swap_out copies a request's blocks device -> host, swap_in host -> device)
+ * and the block-table role ③ of "vLLM Continuous Batching：从 Forward Shape
+ * 理解两个核心参数" §2.3补充.  For each pair (s, d) of pairs (int32
+ * [num_pairs, 2], device memory):
+ *   dst_k[d] = src_k[s] and dst_v[d] = src_v[s], all block_size slots, bit-exact.
+ * Both pools have the [blocks, block_size, num_kv_heads, head_dim] bf16
+ * layout, 16-byte aligned; the caller owns all five buffers.  Each pool
+ * pointer may be device memory, managed memory, or page-locked host memory
+ * (cudaHostAlloc / cudaHostRegister; the kernel uses its mapped device
+ * address); other host memory only where the device reports coherent
+ * pageable-memory access.  A pool pointer the device cannot reach returns
+ * PA_ERR_INVALID_ARG before any launch.  The copy is one kernel reading and
+ * writing through those pointers, so no staging buffer is made.  Destination
+ * blocks must be distinct and must not be source blocks of the same call.
+ * A pair naming a block outside its pool sets PA_DEV_BAD_PAIR and copies
+ * nothing for that pair.  num_pairs == 0 launches nothing; more than 65535
+ * pairs returns PA_ERR_UNSUPPORTED (split the call).
+ */
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                   const int32_t* pairs, int num_pairs, int src_num_blocks, int dst_num_blocks,
+                   int block_size, int num_kv_heads, int head_dim, uint32_t* err_flag,
+                   void* stream);
+
+/*
  * pa_attention_noalloc — pa_attention without a workspace argument, for
  * callers that cannot allocate device memory (a library embedded in a host
  * application that owns every device allocation, a runtime whose memory is

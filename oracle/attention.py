@@ -47,6 +47,21 @@ def copy_blocks(k_cache, v_cache, pairs):
     return kc, vc
 
 
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs):
+    """Move whole blocks between two pools; returns the new destination pools.
+
+    "LLM 推理引擎 Continuous Batching 与 PagedAttention：从 vLLM 原理到生产级部署实战"
+    §4.4: swapping a request out copies its blocks from the GPU pool to the CPU
+    pool, swapping in copies them back; a block is moved whole, all slots.
+    """
+    dk = np.array(dst_k, copy=True)
+    dv = np.array(dst_v, copy=True)
+    for s, d in np.asarray(pairs, dtype=np.int64).reshape(-1, 2).tolist():
+        dk[d] = src_k[s]
+        dv[d] = src_v[s]
+    return dk, dv
+
+
 def gather_sequence(cache, block_table_row, seq_len: int, block_size: int):
     """Dense ``[seq_len, kv_heads, head_dim]`` view of one sequence's paged K or V.
 

@@ -16,7 +16,7 @@ import ctypes
 import math
 import os
 
-__all__ = ["write_kv", "attention", "attention_noalloc", "copy_blocks", "workspace_size", "kernel_launches",
+__all__ = ["write_kv", "attention", "attention_noalloc", "copy_blocks", "swap_blocks", "workspace_size", "kernel_launches",
            "library_path", "load", "PaError", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN",
            "DEV_BAD_DECODE", "DEV_BAD_PAIR"]
 
@@ -47,6 +47,8 @@ _SIGNATURES = {
     "pa_attention_noalloc": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i,
                                     _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
                                     _c_f, _c_p, _c_p]),
+    "pa_swap_blocks": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
+                              _c_p, _c_p]),
     "pa_status_string": (ctypes.c_char_p, [_c_i]),
     "pa_last_cuda_error": (_c_i, []),
     "pa_kernel_launches": (ctypes.c_uint64, []),
@@ -154,6 +156,31 @@ def copy_blocks(k_cache, v_cache, pairs, err=None, stream=None):
     rc = load().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), n, nb, bs, hkv, d,
                                _ptr(err), _stream(stream))
     _check(rc, "pa_copy_blocks")
+
+
+def _pool(t, name):
+    import torch
+    _need(t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4,
+          f"{name} must be a contiguous bf16 tensor [blocks, block_size, kv_heads, head_dim]")
+    _need(t.is_cuda or t.is_pinned(), f"{name} must be on the GPU or in pinned host memory")
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs, err=None, stream=None):
+    """Move whole blocks between pools: ``dst[d] = src[s]`` for each row (s, d) of ``pairs``.
+
+    Either pool may be in pinned host memory (CPU offload of the cache); the
+    copy runs as one kernel reading and writing through the pointers.
+    """
+    for t, n in ((src_k, "src_k"), (src_v, "src_v"), (dst_k, "dst_k"), (dst_v, "dst_v")):
+        _pool(t, n)
+    _i32(pairs, "pairs")
+    _need(src_k.shape == src_v.shape and dst_k.shape == dst_v.shape, "K and V pools differ")
+    _need(src_k.shape[1:] == dst_k.shape[1:], "pools differ in block shape")
+    nsrc, bs, hkv, d = src_k.shape
+    n = pairs.numel() // 2
+    rc = load().pa_swap_blocks(_ptr(src_k), _ptr(src_v), _ptr(dst_k), _ptr(dst_v), _ptr(pairs), n,
+                               nsrc, dst_k.shape[0], bs, hkv, d, _ptr(err), _stream(stream))
+    _check(rc, "pa_swap_blocks")
 
 
 def workspace_size(num_decode_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len) -> int:

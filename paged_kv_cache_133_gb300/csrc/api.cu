@@ -150,6 +150,57 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
                                         static_cast<cudaStream_t>(stream)));
 }
 
+// The address a kernel on the current device uses for `p`, or nullptr when the
+// device cannot reach it: device and managed memory as is, page-locked host
+// memory through its mapped device address, other host memory only where the
+// device reads pageable memory coherently.
+static const void* device_view(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      return p;
+    case cudaMemoryTypeHost:
+      return at.devicePointer;
+    default: {
+      int dev = 0, pageable = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess)
+        return nullptr;
+      return pageable ? p : nullptr;
+    }
+  }
+}
+
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                   const int32_t* pairs, int num_pairs, int src_num_blocks, int dst_num_blocks,
+                   int block_size, int num_kv_heads, int head_dim, uint32_t* err_flag,
+                   void* stream) {
+  if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || block_size <= 0 ||
+      num_kv_heads <= 0 || head_dim <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!src_k || !src_v || !dst_k || !dst_v || (num_pairs > 0 && !pairs)) return PA_ERR_INVALID_ARG;
+  if (num_pairs > 65535) return PA_ERR_UNSUPPORTED;
+  const int64_t elems = static_cast<int64_t>(block_size) * num_kv_heads * head_dim;
+  if (elems % 8 || elems > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
+    return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  const void* sk = device_view(src_k);
+  const void* sv = device_view(src_v);
+  const void* dk = device_view(dst_k);
+  const void* dv = device_view(dst_v);
+  if (!sk || !sv || !dk || !dv) return PA_ERR_INVALID_ARG;
+  return cuda_status(launch_swap_blocks(sk, sv, const_cast<void*>(dk), const_cast<void*>(dv), pairs,
+                                        num_pairs, src_num_blocks, dst_num_blocks,
+                                        static_cast<int>(elems), err_flag,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 size_t pa_attention_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv_heads,
                                    int head_dim, int max_seq_len) {
   int part, nsplit;

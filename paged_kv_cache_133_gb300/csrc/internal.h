@@ -58,6 +58,9 @@ cudaError_t launch_write_kv(const void* k, const void* v, int64_t ks, int64_t vs
                             int row_elems, uint32_t* err, cudaStream_t st);
 cudaError_t launch_copy_blocks(void* kc, void* vc, const int32_t* pairs, int n, int num_blocks,
                                int block_elems, uint32_t* err, cudaStream_t st);
+cudaError_t launch_swap_blocks(const void* sk, const void* sv, void* dk, void* dv,
+                               const int32_t* pairs, int n, int src_blocks, int dst_blocks,
+                               int block_elems, uint32_t* err, cudaStream_t st);
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t st);
 

@@ -62,6 +62,32 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ kc
   }
 }
 
+// Block moves between two pools (blockIdx.y = pair); either pool may live in
+// host memory the device can reach.  Same 16-byte streaming as the block copy.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const uint4* __restrict__ sk,
+                                                          const uint4* __restrict__ sv,
+                                                          uint4* __restrict__ dk,
+                                                          uint4* __restrict__ dv,
+                                                          const int32_t* __restrict__ pairs,
+                                                          int src_blocks, int dst_blocks,
+                                                          int vec_per_block, uint32_t* err) {
+  const int p = blockIdx.y;
+  const int src = __ldg(pairs + 2 * p), dst = __ldg(pairs + 2 * p + 1);
+  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, PA_DEV_BAD_PAIR);
+    return;
+  }
+  const int64_t so = static_cast<int64_t>(src) * vec_per_block;
+  const int64_t d = static_cast<int64_t>(dst) * vec_per_block;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < vec_per_block;
+       i += gridDim.x * blockDim.x) {
+    const uint4 a = sk[so + i];
+    const uint4 b = sv[so + i];
+    dk[d + i] = a;
+    dv[d + i] = b;
+  }
+}
+
 cudaError_t launch_write_kv(const void* k, const void* v, int64_t ks, int64_t vs, void* kc,
                             void* vc, const int32_t* slots, int T, int num_blocks, int bs,
                             int row_elems, uint32_t* err, cudaStream_t st) {
@@ -87,6 +113,20 @@ cudaError_t launch_copy_blocks(void* kc, void* vc, const int32_t* pairs, int n, 
   count_launch();
   copy_blocks_kernel<<<dim3(bx, n), 256, 0, st>>>(static_cast<uint4*>(kc), static_cast<uint4*>(vc),
                                                    pairs, num_blocks, vpb, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swap_blocks(const void* sk, const void* sv, void* dk, void* dv,
+                               const int32_t* pairs, int n, int src_blocks, int dst_blocks,
+                               int block_elems, uint32_t* err, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int vpb = block_elems / 8;
+  int bx = (vpb + 255) / 256;
+  if (bx > 8) bx = 8;
+  count_launch();
+  swap_blocks_kernel<<<dim3(bx, n), 256, 0, st>>>(
+      static_cast<const uint4*>(sk), static_cast<const uint4*>(sv), static_cast<uint4*>(dk),
+      static_cast<uint4*>(dv), pairs, src_blocks, dst_blocks, vpb, err);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 import paged_kv_cache_133_gb300 as pa
 from paged_kv_cache_133_gb300 import build as pabuild
@@ -36,7 +37,8 @@ def lib():
 
 def test_header_declares_the_three_calls():
     names = _declared()
-    for n in ("pa_write_kv", "pa_attention", "pa_attention_workspace_size", "pa_copy_blocks"):
+    for n in ("pa_write_kv", "pa_attention", "pa_attention_workspace_size", "pa_copy_blocks",
+              "pa_swap_blocks"):
         assert n in names
 
 
@@ -83,4 +85,16 @@ def test_host_validation_rejects_before_launch(lib):
     before = lib.pa_kernel_launches()
     assert lib.pa_write_kv(nul, nul, 512, 512, fake, fake, nul, 0, 8, 16, 4, 128, nul, nul) == 0
     assert lib.pa_copy_blocks(fake, fake, nul, 0, 8, 16, 4, 128, nul, nul) == 0
+    assert lib.pa_swap_blocks(fake, fake, fake, fake, nul, 0, 8, 4, 16, 4, 128, nul, nul) == 0
     assert lib.pa_kernel_launches() == before
+    # swap: null pool, empty destination pool, too many pairs for one call
+    assert lib.pa_swap_blocks(fake, nul, fake, fake, fake, 1, 8, 4, 16, 4, 128, nul, nul) == 1
+    assert lib.pa_swap_blocks(fake, fake, fake, fake, fake, 1, 8, 0, 16, 4, 128, nul, nul) == 1
+    assert lib.pa_swap_blocks(fake, fake, fake, fake, fake, 70000, 8, 4, 16, 4, 128, nul, nul) == 2
+
+
+def test_swap_binding_refuses_pageable_host_pools():
+    # Only device memory or page-locked host memory reaches the C call.
+    t = torch.zeros((2, 1, 1, 8), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="pinned"):
+        pa.swap_blocks(t, t, t, t, None)

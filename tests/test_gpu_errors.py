@@ -99,6 +99,20 @@ def test_bad_copy_pair_sets_flag():
     assert torch.equal(before, g["k_cache"])
 
 
+def test_bad_swap_pair_sets_flag():
+    shape = (4, 16, 2, 64)
+    src = torch.randn(shape, device=DEV).to(torch.bfloat16)
+    dk = torch.zeros(shape, dtype=torch.bfloat16).pin_memory()
+    dv = torch.zeros(shape, dtype=torch.bfloat16).pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pairs = torch.tensor([[0, 4], [4, 1], [-1, 2], [2, 3]], dtype=torch.int32, device=DEV)
+    pa.swap_blocks(src, src, dk, dv, pairs, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.DEV_BAD_PAIR
+    assert torch.equal(dk[3], src[2].cpu())               # the valid pair still moved
+    assert not dk[:3].any() and not dv[:3].any()
+
+
 def test_workspace_too_small_is_refused():
     lay = workloads.custom_layout("splits", [20000], [1], 8, 1, 128, 16, 1300, 8)
     g, md, err = _setup(lay)

@@ -228,6 +228,54 @@ def test_copy_blocks_pages_example():
     assert np.array_equal(kc[keep], cache[keep])
 
 
+def test_swap_out_and_in_round_trip():
+    # §4.4 of the deployment page: blocks go device -> host on swap-out and
+    # come back host -> device (into whatever blocks are free) on swap-in.
+    rng = np.random.default_rng(5)
+    gpu = rng.integers(-1000, 1000, size=(10, 4, 2, 3)).astype(np.int16)
+    cpu = rng.integers(-1000, 1000, size=(6, 4, 2, 3)).astype(np.int16)
+    gpu_before, cpu_before = gpu.copy(), cpu.copy()
+    out_pairs = [[3, 0], [5, 4], [1, 2]]
+    hk, hv = ref.swap_blocks(gpu, -gpu, cpu, -cpu, out_pairs)
+    assert np.array_equal(gpu, gpu_before) and np.array_equal(cpu, cpu_before)   # inputs kept
+    for s, d in out_pairs:
+        assert np.array_equal(hk[d], gpu[s]) and np.array_equal(hv[d], -gpu[s])
+    for b in (1, 3, 5):                                   # host blocks no pair names
+        assert np.array_equal(hk[b], cpu[b])
+    in_pairs = [[0, 7], [4, 6], [2, 9]]
+    dk, dv = ref.swap_blocks(hk, hv, gpu, -gpu, in_pairs)
+    for (g_src, _), (_, g_dst) in zip(out_pairs, in_pairs):
+        assert np.array_equal(dk[g_dst], gpu[g_src]) and np.array_equal(dv[g_dst], -gpu[g_src])
+    for b in (0, 1, 2, 3, 4, 5, 8):
+        assert np.array_equal(dk[b], gpu[b])
+
+
+def test_swap_in_to_other_blocks_keeps_attention():
+    # The block table is the only link from positions to blocks: after B's
+    # blocks (10, 21 in the worked step) leave for the host and come back
+    # into blocks 30, 31, attention with B's table rewritten is unchanged.
+    ex = GOLDEN["bca_step"]
+    rng = np.random.default_rng(9)
+    nb, bs, hkv, d = 40, ex["block_size"], 2, 8
+    kc = rng.standard_normal((nb, bs, hkv, d))
+    vc = rng.standard_normal((nb, bs, hkv, d))
+    q = rng.standard_normal((7, 4, d))
+    tables = [ex["tables"]["B"], [7], ex["tables"]["A"]]
+    bt = metadata.pad_block_tables(tables)
+    args = (ex["query_start_loc"], ex["seq_lens"])
+    before = ref.attention(q, kc, vc, *args, bt, bs, 0.3, hkv)
+    host_k = np.zeros((4, bs, hkv, d))
+    host_v = np.zeros((4, bs, hkv, d))
+    host_k, host_v = ref.swap_blocks(kc, vc, host_k, host_v, [[10, 2], [21, 0]])
+    kc2, vc2 = kc.copy(), vc.copy()
+    kc2[[10, 21]] = np.nan                                  # freed, then reused by others
+    vc2[[10, 21]] = np.nan
+    kc2, vc2 = ref.swap_blocks(host_k, host_v, kc2, vc2, [[2, 30], [0, 31]])
+    bt2 = metadata.pad_block_tables([[30, 31], [7], ex["tables"]["A"]])
+    after = ref.attention(q, kc2, vc2, *args, bt2, bs, 0.3, hkv)
+    assert np.array_equal(before, after)
+
+
 def test_attention_flops_closed_form():
     # decode with history c: q=1 sees c+1 keys; prefill of n sees n(n+1)/2 pairs
     assert ref.attention_flops([0, 1], [8], 1, 1) == 4 * 8
