@@ -83,6 +83,36 @@ constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
+// ---- fp32 pairs ------------------------------------------------------------------
+// The softmax works on pairs of scores with the f32x2 add / fma instructions
+// of this architecture, and takes row maxima three operands at a time; both
+// cut its instruction count, which (not the exponential unit) bounds it.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int D>
 struct PpLayout {
   static constexpr int kHalves = D / 64;        // 64-element (128-byte) column chunks
@@ -436,49 +466,49 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
         tmem_wait_ld();
-        float mx[8];
-#pragma unroll
-        for (int x = 0; x < 8; ++x) mx[x] = -INFINITY;
-        if (full) {
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int e2 = 0; e2 < 32; ++e2) {
-              const float v = __uint_as_float(sr[cc][e2]) * a.scale_log2;
-              mx[e2 & 7] = fmaxf(mx[e2 & 7], v);
-            }
-        } else {
+        // Row maximum of the raw scores (scale > 0, so it commutes with the
+        // scaling); masked keys become -inf.
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (!full) {
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
             for (int e2 = 0; e2 < 32; ++e2) {
               const int pos = key0 + cc * 32 + e2;
-              float v = __uint_as_float(sr[cc][e2]) * a.scale_log2;
-              if (pos > lim || pos >= I.kv_end) v = -INFINITY;
-              sr[cc][e2] = __float_as_uint(v);
-              mx[e2 & 7] = fmaxf(mx[e2 & 7], v);
+              if (pos > lim || pos >= I.kv_end) sr[cc][e2] = __float_as_uint(-INFINITY);
             }
         }
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int e2 = 0; e2 < 32; e2 += 8) {
+            const int q = (e2 >> 3) & 3;
+            mx[q] = max3(mx[q], __uint_as_float(sr[cc][e2]), __uint_as_float(sr[cc][e2 + 1]));
+            mx[q] = max3(mx[q], __uint_as_float(sr[cc][e2 + 2]), __uint_as_float(sr[cc][e2 + 3]));
+            mx[q] = max3(mx[q], __uint_as_float(sr[cc][e2 + 4]), __uint_as_float(sr[cc][e2 + 5]));
+            mx[q] = max3(mx[q], __uint_as_float(sr[cc][e2 + 6]), __uint_as_float(sr[cc][e2 + 7]));
+          }
+        const float mt = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]) * a.scale_log2;
         const float m_new = mt > m_used + 8.f ? mt : m_used;
         const float ref = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - ref);
-        // P = 2^(s - m), rounded to bf16 and packed in pairs into sr[0..1]
-        const float mul = full ? a.scale_log2 : 1.f;
-        float sm[8];
-#pragma unroll
-        for (int x = 0; x < 8; ++x) sm[x] = 0.f;
+        // P = 2^(s * scale - m), rounded to bf16 and packed in pairs into sr[0..1]
+        const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
+        const uint64_t nref2 = f2(-ref, -ref);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // four (+0, +0) pair sums
         uint32_t* flat = &sr[0][0];
 #pragma unroll
         for (int e2 = 0; e2 < 128; e2 += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(flat[e2]), mul, -ref));
-          const float p1 = ex2(fmaf(__uint_as_float(flat[e2 + 1]), mul, -ref));
-          sm[e2 & 7] += p0;
-          sm[(e2 + 1) & 7] += p1;
-          flat[e2 >> 1] = pack_bf16(p0, p1);
+          const uint64_t x = f2_fma(f2(__uint_as_float(flat[e2]), __uint_as_float(flat[e2 + 1])),
+                                    sc2, nref2);
+          const float2 xc = f2_split(x);
+          const uint64_t pp = f2(ex2(xc.x), ex2(xc.y));
+          acc[(e2 >> 1) & 3] = f2_add(acc[(e2 >> 1) & 3], pp);
+          const float2 pc = f2_split(pp);
+          flat[e2 >> 1] = pack_bf16(pc.x, pc.y);
         }
-        l = l * alpha + (((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7])));
+        const float2 s01 = f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
+        l = l * alpha + (s01.x + s01.y);
         tmem_st32(tS, sr[0]);
         tmem_st32(tS + 32, sr[1]);
         const bool need = j > 0 && m_new != m_used;
@@ -629,6 +659,7 @@ bool prefill_tc_supported(const AttnArgs& a) {
   const char* env = getenv("PA_PREFILL_IMPL");
   if (env && strcmp(env, "mma") == 0) return false;
   if (a.head_dim != 64 && a.head_dim != 128) return false;
+  if (!(a.scale_log2 > 0.f)) return false;  // the row maximum is taken before scaling
   if (a.bs_log2 < 3) return false;  // TMA boxes of >= 8 rows keep 1 KB swizzle alignment
   if ((a.q_stride * 2) % 16 != 0) return false;
   if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k_cache) |

@@ -51,6 +51,12 @@ def _small_cases():
     # degenerate: single-token prompts (L = 1), and an empty sequence in the middle
     cases.append(workloads.custom_layout("L1", [0, 0, 5], [1, 1, 1], 4, 2, 128, 16, 8, 3))
     cases.append(workloads.custom_layout("empty_mid", [9, 3, 0], [1, 0, 17], 4, 1, 64, 4, 16, 4))
+    # scale <= 0 is legal (the tensor-core prefill takes the row maximum before
+    # scaling and leaves such steps to the general kernel)
+    cases.append(workloads.custom_layout("neg_scale", [40, 0, 130], [1, 150, 70], 8, 2, 128, 16,
+                                         40, 5, scale=-0.07))
+    cases.append(workloads.custom_layout("zero_scale", [0, 20], [90, 33], 4, 2, 64, 16, 16, 6,
+                                         scale=0.0))
     return cases
 
 
