@@ -21,7 +21,7 @@
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3   softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
 //   warps 4-7   softmax + epilogue of tile B
-//   warp 8      TMA producer of K_j (3-stage ring)
+//   warp 8      TMA producer of K_j (2-stage ring)
 //   warp 9      TMEM allocation and MMA issue (one lane)
 //   warp 10     TMA producer of V_j (2-stage ring)
 //   warp 11     scheduler: draws items from the global queue, hands them to the
@@ -118,20 +118,21 @@ struct PpLayout {
   static constexpr int kHalves = D / 64;        // 64-element (128-byte) column chunks
   static constexpr int kHalf = kM * 128;         // one chunk of a 128-row tile: 16 KB
   static constexpr int kTile = kHalves * kHalf;  // Q, K or V tile
-  static constexpr int kKStages = 3;
+  static constexpr int kKStages = 2;
   static constexpr int kVStages = 2;
   static constexpr int kQA = 0;
   static constexpr int kQB = kTile;
   static constexpr int kK = 2 * kTile;
   static constexpr int kV = kK + kKStages * kTile;
-  static constexpr int kBar = kV + kVStages * kTile;
+  static constexpr int kStage = kV + kVStages * kTile;  // output staging, 4 KB per softmax warp
+  static constexpr int kBar = kStage + kSoftmaxWarps * 4096;
   static constexpr int kBytes = kBar + 512;  // barriers, TMEM slot, flags, item ring
   static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1 KB
 };
 
 enum : int {
   bQFull, bQFree,
-  bKFull0, bKFull1, bKFull2, bKEmpty0, bKEmpty1, bKEmpty2,
+  bKFull0, bKFull1, bKEmpty0, bKEmpty1,
   bVFull0, bVFull1, bVEmpty0, bVEmpty1,
   bSA, bSB, bPA, bPB, bPvA, bPvB, bOFreeA, bOFreeB, bDrain,
   bItemFull0, bItemFull1, bItemEmpty0, bItemEmpty1, kNumBars
@@ -347,24 +348,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_bf16(kM, kN, false);
     constexpr uint32_t kIdO = idesc_bf16(kM, D, true);
+    // Shared-memory descriptors are built once; a K step or a stage moves the
+    // start address, which sits in the descriptor's low bits (address >> 4),
+    // so each product costs one add per operand.  (The issuing lane shares its
+    // sub-partition with two softmax warps, so every instruction it saves
+    // shortens the gap between a P being ready and its product starting.)
+    const uint64_t dQA = smem_desc_sw128(base + Ly::kQA, 16, 1024);
+    const uint64_t dQB = smem_desc_sw128(base + Ly::kQB, 16, 1024);
+    const uint64_t dK0 = smem_desc_sw128(base + Ly::kK, 16, 1024);
+    const uint64_t dV0 = smem_desc_sw128(base + Ly::kV, Ly::kHalf, 1024);
+    const uint32_t tS0 = tmem, tO0 = tmem + 256;
     auto issue_s = [&](int side, int g) {
-      const uint32_t q0 = base + (side ? Ly::kQB : Ly::kQA);
-      const uint32_t k0 = base + Ly::kK + (g % Ly::kKStages) * Ly::kTile;
+      const uint64_t a0 = side ? dQB : dQA;
+      const uint64_t b0 = dK0 + static_cast<uint64_t>((g % Ly::kKStages) * (Ly::kTile >> 4));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * Ly::kHalf + (kk & 3) * 32;
-        mma_f16_ss(tmem + side * 128, smem_desc_sw128(q0 + off, 16, 1024),
-                   smem_desc_sw128(k0 + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * Ly::kHalf + (kk & 3) * 32) >> 4);
+        mma_f16_ss(tS0 + side * 128, a0 + off, b0 + off, kIdS, kk > 0 ? 1u : 0u);
       }
       mma_commit(BAR(side ? bSB : bSA));
     };
     auto issue_pv = [&](int side, int g, bool acc) {
-      const uint32_t v0 = base + Ly::kV + (g % Ly::kVStages) * Ly::kTile;
+      const uint64_t v0 = dV0 + static_cast<uint64_t>((g % Ly::kVStages) * (Ly::kTile >> 4));
 #pragma unroll
       for (int kk = 0; kk < kN / 16; ++kk)
-        mma_f16_ts(tmem + 256 + side * 128, tmem + side * 128 + kk * 8,
-                   smem_desc_sw128(v0 + kk * 2048, Ly::kHalf, 1024), kIdO,
-                   (acc || kk > 0) ? 1u : 0u);
+        mma_f16_ts(tO0 + side * 128, tS0 + side * 128 + kk * 8, v0 + static_cast<uint64_t>(kk * (2048 >> 4)),
+                   kIdO, (acc || kk > 0) ? 1u : 0u);
       mma_commit(BAR(side ? bPvB : bPvA));
     };
     int gt = 0, it = 0, gB = 0, itB = 0;
@@ -452,7 +461,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!next_item(k, I, true)) break;
       if (side == 1 && I.h[1] < 0) continue;
       const int i = I.i0 + r;
-      const bool row_ok = i < I.qn;
       const int lim = I.c + i;  // last key position this row sees
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < I.n; ++j) {
@@ -462,32 +470,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int key0 = j * kN;
         const bool full = key0 + kN - 1 <= lim && key0 + kN <= I.kv_end;
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+        uint32_t sr[128];
+        tmem_ld128(tS, sr);
         tmem_wait_ld();
         // Row maximum of the raw scores (scale > 0, so it commutes with the
         // scaling); masked keys become -inf.
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (!full) {
+          const int last = min(lim, I.kv_end - 1) - key0;  // last visible column of this row
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int e2 = 0; e2 < 32; ++e2) {
-              const int pos = key0 + cc * 32 + e2;
-              if (pos > lim || pos >= I.kv_end) sr[cc][e2] = __float_as_uint(-INFINITY);
-            }
+          for (int e2 = 0; e2 < 128; ++e2)
+            if (e2 > last) sr[e2] = __float_as_uint(-INFINITY);
         }
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int e2 = 0; e2 < 32; e2 += 8) {
-            const int q = (e2 >> 3) & 3;
-            mx[q] = max3(mx[q], __uint_as_float(sr[cc][e2]), __uint_as_float(sr[cc][e2 + 1]));
-            mx[q] = max3(mx[q], __uint_as_float(sr[cc][e2 + 2]), __uint_as_float(sr[cc][e2 + 3]));
-            mx[q] = max3(mx[q], __uint_as_float(sr[cc][e2 + 4]), __uint_as_float(sr[cc][e2 + 5]));
-            mx[q] = max3(mx[q], __uint_as_float(sr[cc][e2 + 6]), __uint_as_float(sr[cc][e2 + 7]));
-          }
+        for (int e2 = 0; e2 < 128; e2 += 8) {
+          const int q = (e2 >> 3) & 3;
+          mx[q] = max3(mx[q], __uint_as_float(sr[e2]), __uint_as_float(sr[e2 + 1]));
+          mx[q] = max3(mx[q], __uint_as_float(sr[e2 + 2]), __uint_as_float(sr[e2 + 3]));
+          mx[q] = max3(mx[q], __uint_as_float(sr[e2 + 4]), __uint_as_float(sr[e2 + 5]));
+          mx[q] = max3(mx[q], __uint_as_float(sr[e2 + 6]), __uint_as_float(sr[e2 + 7]));
+        }
         const float mt = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]) * a.scale_log2;
         const float m_new = mt > m_used + 8.f ? mt : m_used;
         const float ref = m_new == -INFINITY ? 0.f : m_new;
@@ -496,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
         const uint64_t nref2 = f2(-ref, -ref);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // four (+0, +0) pair sums
-        uint32_t* flat = &sr[0][0];
+        uint32_t* flat = sr;
 #pragma unroll
         for (int e2 = 0; e2 < 128; e2 += 2) {
           const uint64_t x = f2_fma(f2(__uint_as_float(flat[e2]), __uint_as_float(flat[e2 + 1])),
@@ -509,8 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float2 s01 = f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
         l = l * alpha + (s01.x + s01.y);
-        tmem_st32(tS, sr[0]);
-        tmem_st32(tS + 32, sr[1]);
+        tmem_st64(tS, *reinterpret_cast<uint32_t(*)[64]>(sr));
         const bool need = j > 0 && m_new != m_used;
         if (__any_sync(0xffffffffu, need)) {
           const float f = need ? alpha : 1.f;
@@ -530,20 +531,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(BAR(side ? bPB : bPA));
       }
       if (!ok) break;
-      // epilogue: wait for this side's last product, normalise, store
+      // epilogue: wait for this side's last product, normalise, store.  Each
+      // warp stages 64 columns of its 32 rows (128 B per row, 16-byte pieces
+      // XOR-swizzled by row) in its own 4 KB of shared memory and writes them
+      // back four rows per instruction, so a store covers whole 128-byte row
+      // segments rather than 32 scattered 16-byte pieces.
       if (!(ok = wait(side ? bPvB : bPvA, gx + I.n - 1))) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                            static_cast<int64_t>(I.t0 + (row_ok ? i : 0)) * a.out_stride +
-                            static_cast<int64_t>(I.h[side]) * D;
+      uint8_t* stg = sgen + Ly::kStage + warp * 4096;
+      const int wrow0 = I.i0 + (warp & 3) * 32;  // query row of this warp's lane 0
+      __nv_bfloat16* ohead = static_cast<__nv_bfloat16*>(a.out) +
+                             static_cast<int64_t>(I.h[side]) * D;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tO + cc * 32, o);
-        tmem_wait_ld();
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+      for (int hh = 0; hh < D / 64; ++hh) {
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t o[32];
+          tmem_ld32(tO + hh * 64 + c2 * 32, o);
+          tmem_wait_ld();
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
@@ -551,9 +557,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             w.y = pack_bf16(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
             w.z = pack_bf16(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
             w.w = pack_bf16(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-            dst[q4] = w;
+            const int piece = c2 * 4 + q4;
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((piece ^ (lane & 7)) << 4)) = w;
           }
         }
+        __syncwarp();
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const int rr = i4 * 4 + (lane >> 3);  // row within the warp's 32
+          const int piece = lane & 7;
+          const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((piece ^ (rr & 7)) << 4));
+          const int qi = wrow0 + rr;
+          if (qi < I.qn)
+            *reinterpret_cast<uint4*>(ohead + static_cast<int64_t>(I.t0 + qi) * a.out_stride +
+                                      hh * 64 + piece * 8) = w;
+        }
+        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(BAR(side ? bOFreeB : bOFreeA));
