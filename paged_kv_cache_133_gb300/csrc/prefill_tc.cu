@@ -192,7 +192,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, const AttnArgs a,
                       int total_slots, int max_level) {
   using Ly = PpLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -226,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -237,8 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     flag_error(a.err, PA_DEV_TIMEOUT);
   };
   auto wait = [&](int b, int completion) -> bool {
+    const uint32_t parity = static_cast<uint32_t>(completion) & 1u;
+    if (mbar_try_wait(BAR(b), parity)) return true;
     if (*abort_flag) return false;
-    if (mbar_wait(BAR(b), static_cast<uint32_t>(completion) & 1u, kWaitNs)) return true;
+    if (mbar_wait(BAR(b), parity, kWaitNs)) return true;
     give_up();
     return false;
   };
@@ -374,78 +378,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < kN / 16; ++kk)
         mma_f16_ts(tO0 + side * 128, tS0 + side * 128 + kk * 8, v0 + static_cast<uint64_t>(kk * (2048 >> 4)),
                    kIdO, (acc || kk > 0) ? 1u : 0u);
-      mma_commit(BAR(side ? bPvB : bPvA));
     };
-    int gt = 0, it = 0, gB = 0, itB = 0;
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      Item I;
-      if (!next_item(k, I, false)) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(bItemEmpty0 + (k & 1)));
-      const bool hasB = I.h[1] >= 0;
-      if (!(ok = wait(bQFull, it) && wait(bKFull0 + gt % Ly::kKStages, gt / Ly::kKStages))) break;
-      tc_fence_after();
-      if (lane == 0) {
+    // One lane issues everything; the V rows past the last key of a partial
+    // tile are zeroed by softmax A before it reports its P.
+    if (lane == 0) {
+      int gt = 0, it = 0, gB = 0, itB = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        Item I;
+        if (!next_item(k, I, true)) break;
+        const bool hasB = I.h[1] >= 0;
+        if (!(ok = wait(bQFull, it) && wait(bKFull0 + gt % Ly::kKStages, gt / Ly::kKStages))) break;
+        tc_fence_after();
         issue_s(0, gt);
         if (hasB) issue_s(1, gt);
         mma_commit(BAR(bKEmpty0 + gt % Ly::kKStages));
         if (I.n == 1) mma_commit(BAR(bQFree));
-      }
-      __syncwarp();
-      for (int j = 0; j < I.n; ++j) {
-        const int g = gt + j;
-        const bool more = j + 1 < I.n;
-        ok = wait(bPA, g) && (j > 0 || it == 0 || wait(bOFreeA, it - 1)) &&
-             wait(bVFull0 + g % Ly::kVStages, g / Ly::kVStages);
-        if (!ok) break;
-        tc_fence_after();
-        const int live = I.kv_end - j * kN;  // rows [live, 128) of V_j are not keys
-        if (live < kN) {
-          uint8_t* vt = sgen + Ly::kV + (g % Ly::kVStages) * Ly::kTile;
-          const int chunks = (kN - live) * 128 / 16;
-          for (int hf = 0; hf < Ly::kHalves; ++hf) {
-            uint4* p = reinterpret_cast<uint4*>(vt + hf * Ly::kHalf + live * 128);
-            for (int x = lane; x < chunks; x += 32) p[x] = make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < I.n; ++j) {
+          const int g = gt + j;
+          const bool more = j + 1 < I.n;
+          ok = wait(bPA, g) && (j > 0 || it == 0 || wait(bOFreeA, it - 1)) &&
+               wait(bVFull0 + g % Ly::kVStages, g / Ly::kVStages);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(0, g, j > 0);
+          if (more) {
+            if (!(ok = wait(bKFull0 + (g + 1) % Ly::kKStages, (g + 1) / Ly::kKStages))) break;
+            tc_fence_after();
+            issue_s(0, g + 1);
           }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) issue_pv(0, g, j > 0);
-        __syncwarp();
-        if (more) {
-          if (!(ok = wait(bKFull0 + (g + 1) % Ly::kKStages, (g + 1) / Ly::kKStages))) break;
-          tc_fence_after();
-          if (lane == 0) issue_s(0, g + 1);
-          __syncwarp();
-        }
-        if (hasB) {
-          if (!(ok = wait(bPB, gB + j) && (j > 0 || itB == 0 || wait(bOFreeB, itB - 1)))) break;
-          tc_fence_after();
-          if (lane == 0) {
+          if (hasB) {
+            if (!(ok = wait(bPB, gB + j) && (j > 0 || itB == 0 || wait(bOFreeB, itB - 1)))) break;
+            tc_fence_after();
             issue_pv(1, g, j > 0);
             if (more) issue_s(1, g + 1);
           }
-          __syncwarp();
-        }
-        if (lane == 0) {
+          if (!more) {  // the item's O products are all issued
+            mma_commit(BAR(bPvA));
+            if (hasB) mma_commit(BAR(bPvB));
+          }
           mma_commit(BAR(bVEmpty0 + g % Ly::kVStages));
           if (more) mma_commit(BAR(bKEmpty0 + (g + 1) % Ly::kKStages));
           if (j + 2 == I.n) mma_commit(BAR(bQFree));  // the item's last S products are issued
         }
-        __syncwarp();
+        if (!ok) break;
+        gt += I.n;
+        ++it;
+        if (hasB) {
+          gB += I.n;
+          ++itB;
+        }
       }
-      if (!ok) break;
-      gt += I.n;
-      ++it;
-      if (hasB) {
-        gB += I.n;
-        ++itB;
-      }
+      mma_commit(BAR(bDrain));
+      mbar_wait(BAR(bDrain), 0, kWaitNs);
     }
-    if (lane == 0) mma_commit(BAR(bDrain));
     __syncwarp();
-    mbar_wait(BAR(bDrain), 0, kWaitNs);
   } else if (warp < kProducerWarp) {
     // ------------------------------------------------------------ softmax A / B
     regs_increase<200>();
@@ -455,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + side * 128 + lane_off;
     const uint32_t tO = tmem + 256 + side * 128 + lane_off;
     int gx = 0;  // tiles this side has processed
+    int ix = 0;  // items this side has processed
     bool ok = true;
     for (int k = 0; ok; ++k) {
       Item I;
@@ -526,58 +514,87 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         m_used = m_new;
+        const int live = I.kv_end - key0;  // rows [live, 128) of V_j are not keys
+        if (side == 0 && live < kN) {
+          if (!(ok = wait(bVFull0 + (gx + j) % Ly::kVStages, (gx + j) / Ly::kVStages))) break;
+          uint8_t* vt = sgen + Ly::kV + ((gx + j) % Ly::kVStages) * Ly::kTile;
+          const int chunks = (kN - live) * 128 / 16;
+          for (int hf = 0; hf < Ly::kHalves; ++hf) {
+            uint4* zp = reinterpret_cast<uint4*>(vt + hf * Ly::kHalf + live * 128);
+            for (int x = r; x < chunks; x += 128) zp[x] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(BAR(side ? bPB : bPA));
       }
       if (!ok) break;
-      // epilogue: wait for this side's last product, normalise, store.  Each
-      // warp stages 64 columns of its 32 rows (128 B per row, 16-byte pieces
-      // XOR-swizzled by row) in its own 4 KB of shared memory and writes them
-      // back four rows per instruction, so a store covers whole 128-byte row
-      // segments rather than 32 scattered 16-byte pieces.
-      if (!(ok = wait(side ? bPvB : bPvA, gx + I.n - 1))) break;
+      // epilogue: wait for this side's last product and read O out of TMEM;
+      // release O to the next item's products at once, then normalise, pack
+      // and store from registers.  Each warp stages 64 columns of its 32 rows
+      // (128 B per row, 16-byte pieces XOR-swizzled by row: the TMA 128-byte
+      // swizzle) in its own 4 KB of shared memory; lane 0 writes the block
+      // out with one asynchronous tensor store when all 32 rows are query
+      // rows of this sequence, else the warp stores the live rows itself.
+      if (!(ok = wait(side ? bPvB : bPvA, ix))) break;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint8_t* stg = sgen + Ly::kStage + warp * 4096;
-      const int wrow0 = I.i0 + (warp & 3) * 32;  // query row of this warp's lane 0
-      __nv_bfloat16* ohead = static_cast<__nv_bfloat16*>(a.out) +
-                             static_cast<int64_t>(I.h[side]) * D;
-#pragma unroll 1
-      for (int hh = 0; hh < D / 64; ++hh) {
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t o[32];
-          tmem_ld32(tO + hh * 64 + c2 * 32, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-            const int piece = c2 * 4 + q4;
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((piece ^ (lane & 7)) << 4)) = w;
-          }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const int rr = i4 * 4 + (lane >> 3);  // row within the warp's 32
-          const int piece = lane & 7;
-          const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((piece ^ (rr & 7)) << 4));
-          const int qi = wrow0 + rr;
-          if (qi < I.qn)
-            *reinterpret_cast<uint4*>(ohead + static_cast<int64_t>(I.t0 + qi) * a.out_stride +
-                                      hh * 64 + piece * 8) = w;
-        }
-        __syncwarp();
+      uint32_t o[D];
+      if constexpr (D == 128) {
+        tmem_ld128(tO, o);
+      } else {
+        tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(o));
+        tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
       }
+      tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(BAR(side ? bOFreeB : bOFreeA));
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int e2 = 0; e2 < D / 2; ++e2)
+        o[e2] = pack_bf16(__uint_as_float(o[2 * e2]) * inv, __uint_as_float(o[2 * e2 + 1]) * inv);
+      uint8_t* stg = sgen + Ly::kStage + warp * 4096;
+      const uint32_t stg_s = base + Ly::kStage + warp * 4096;
+      const int wrow0 = I.i0 + (warp & 3) * 32;  // query row of this warp's lane 0
+      const bool whole = wrow0 + 32 <= I.qn;
+      __nv_bfloat16* ohead = static_cast<__nv_bfloat16*>(a.out) +
+                             static_cast<int64_t>(I.h[side]) * D;
+#pragma unroll
+      for (int hh = 0; hh < D / 64; ++hh) {
+        if (lane == 0) bulk_wait_read();  // the previous store has read the staging buffer
+        __syncwarp();
+#pragma unroll
+        for (int piece = 0; piece < 8; ++piece)
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((piece ^ (lane & 7)) << 4)) =
+              make_uint4(o[hh * 32 + piece * 4], o[hh * 32 + piece * 4 + 1],
+                         o[hh * 32 + piece * 4 + 2], o[hh * 32 + piece * 4 + 3]);
+        if (whole) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_o, stg_s, I.h[side] * D + hh * 64, I.t0 + wrow0);
+            bulk_commit();
+          }
+        } else {
+          __syncwarp();
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const int rr = i4 * 4 + (lane >> 3);  // row within the warp's 32
+            const int piece = lane & 7;
+            const uint4 w =
+                *reinterpret_cast<const uint4*>(stg + rr * 128 + ((piece ^ (rr & 7)) << 4));
+            const int qi = wrow0 + rr;
+            if (qi < I.qn)
+              *reinterpret_cast<uint4*>(ohead + static_cast<int64_t>(I.t0 + qi) * a.out_stride +
+                                        hh * 64 + piece * 8) = w;
+          }
+          __syncwarp();
+        }
+      }
       gx += I.n;
+      ++ix;
     }
+    if (lane == 0) bulk_wait();  // every tensor store of this warp is complete
   }
 #undef BAR
   tc_fence_before();
@@ -637,6 +654,19 @@ bool encode_cache(CUtensorMap* m, const void* ptr, const AttnArgs& a) {
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_out(CUtensorMap* m, const AttnArgs& a) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.hq) * a.head_dim,
+                              static_cast<cuuint64_t>(a.num_tokens)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.out_stride) * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t es[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Highest cost level: every visible key range is at most max_seq_len keys.
 int max_level_of(const AttnArgs& a) { return (a.max_seq_len + kN - 1) / kN + 1; }
 
@@ -657,8 +687,9 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  CUtensorMap mq, mk, mv;
-  if (!encode_q(&mq, a) || !encode_cache(&mk, a.k_cache, a) || !encode_cache(&mv, a.v_cache, a))
+  CUtensorMap mq, mk, mv, mo;
+  if (!encode_q(&mq, a) || !encode_cache(&mk, a.k_cache, a) || !encode_cache(&mv, a.v_cache, a) ||
+      !encode_out(&mo, a))
     return cudaErrorNotSupported;  // nothing launched: the caller takes the general kernel
   const int total = static_cast<int>(total_slots_of(a));
   int sms = device_num_sms();
@@ -668,7 +699,7 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
   if (e != cudaSuccess) return e;
   count_launch();
-  prefill_tc_kernel<D><<<grid, kThreads, Ly::kAlloc, st>>>(mq, mk, mv, a, total, max_level_of(a));
+  prefill_tc_kernel<D><<<grid, kThreads, Ly::kAlloc, st>>>(mq, mk, mv, mo, a, total, max_level_of(a));
   return cudaGetLastError();
 }
 
@@ -680,9 +711,9 @@ bool prefill_tc_supported(const AttnArgs& a) {
   if (a.head_dim != 64 && a.head_dim != 128) return false;
   if (!(a.scale_log2 > 0.f)) return false;  // the row maximum is taken before scaling
   if (a.bs_log2 < 3) return false;  // TMA boxes of >= 8 rows keep 1 KB swizzle alignment
-  if ((a.q_stride * 2) % 16 != 0) return false;
+  if ((a.q_stride * 2) % 16 != 0 || (a.out_stride * 2) % 16 != 0) return false;
   if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k_cache) |
-       reinterpret_cast<uintptr_t>(a.v_cache)) & 15u)
+       reinterpret_cast<uintptr_t>(a.v_cache) | reinterpret_cast<uintptr_t>(a.out)) & 15u)
     return false;
   if (total_slots_of(a) > INT_MAX / 2) return false;
   return encode_fn() != nullptr;

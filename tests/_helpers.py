@@ -34,8 +34,21 @@ def device_meta(lay, dev):
     }
 
 
+_ERR = None
+
+
+def default_err():
+    """Error flag used by run_step when the test passes none (zero it, check it after)."""
+    global _ERR
+    if _ERR is None:
+        _ERR = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    return _ERR
+
+
 def run_step(lay, g, md, err=None, num_decode=None, out=None, workspace=None):
     """copy_blocks (if any pairs) -> write_kv -> attention, all on the current stream."""
+    if err is None:
+        err = default_err()
     if len(lay.cow_pairs):
         pa.copy_blocks(g["k_cache"], g["v_cache"], md["pairs"], err=err)
     pa.write_kv(g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"], err=err)

@@ -25,6 +25,15 @@ def _built():
     torch.cuda.set_device(0)
 
 
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    # every step a test runs without its own flag reports here; none may fire
+    H.default_err().zero_()
+    yield
+    torch.cuda.synchronize()
+    assert int(H.default_err().item()) == 0
+
+
 def _small_cases():
     rng = np.random.default_rng(11)
     cases = [workloads.config_layout(1, 0), workloads.literal_layout()]
@@ -276,11 +285,13 @@ def test_prefill_full_size_both_kernels_agree(cfg, monkeypatch):
     lay = workloads.config_layout(cfg, 0)
     g = workloads.make_tensors(lay, seed=0, device=DEV)
     md = H.device_meta(lay, DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
     monkeypatch.delenv("PA_PREFILL_IMPL", raising=False)
-    out_tc = H.run_step(lay, g, md).clone()
+    out_tc = H.run_step(lay, g, md, err=err).clone()
     monkeypatch.setenv("PA_PREFILL_IMPL", "mma")
-    out_mma = H.run_step(lay, g, md).clone()
+    out_mma = H.run_step(lay, g, md, err=err).clone()
     torch.cuda.synchronize()
+    assert int(err.item()) == 0
     rows = slice(lay.num_decode_seqs, None)
     d = (out_tc.float() - out_mma.float()).abs()
     assert torch.isfinite(out_tc.float()).all()
