@@ -382,6 +382,17 @@ def secondary(dev, steps, warmup, peaks):
                       "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16"],
                                    "unit": "TFLOP/s", "frac": tf / peaks["bf16"]}}
     del st
+    lay = workloads.config_layout(6, 0)
+    st = Step(lay, dev)
+    ms6, attn6, _ = time_device(st, steps, warmup, False)
+    fl6 = attention_flops(lay, np.arange(lay.num_seqs))
+    tf6 = fl6 / (attn6 * 1e-3) / 1e12
+    res["prefix"] = {"workload": "32 prefix-cache hits: cached U[1024,8192], new chunks U[64,512], 32q/8kv, D 128, bs 16",
+                     "metric": "prefix-cached prefill TFLOP/s", "value": tf6, "ms_attention": attn6,
+                     "ms_per_step": ms6, "flops": fl6,
+                     "roofline": {"bound": "tensor", "achieved": tf6, "peak": peaks["bf16"],
+                                  "unit": "TFLOP/s", "frac": tf6 / peaks["bf16"]}}
+    del st
     lay = workloads.config_layout(4, 0)
     st = Step(lay, dev)
     ms, attn_ms, _ = time_device(st, steps, warmup, False)
@@ -466,7 +477,7 @@ def swap_leg(dev, iters=20, warmup=3, pairs=4096, seed=0):
 
 def run_other(args, dev, peaks, rank, world, dist_on):
     """One JSON line for the prefill, mixed or shared-prefix workload."""
-    cfg = {"prefill": 3, "mixed": 4, "shared": 5}[args.workload]
+    cfg = {"prefill": 3, "mixed": 4, "shared": 5, "prefix": 6}[args.workload]
     lay = workloads.config_layout(cfg, args.seed)
     step = Step(lay, dev, seed=args.seed + rank)
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
@@ -479,9 +490,10 @@ def run_other(args, dev, peaks, rank, world, dist_on):
         return
     dec = np.arange(lay.num_decode_seqs)
     pre = np.arange(lay.num_decode_seqs, lay.num_seqs)
-    if args.workload == "prefill":
+    if args.workload in ("prefill", "prefix"):
         fl = attention_flops(lay, pre)
-        value, unit, metric = world * fl / (ms * 1e-3) / 1e12, "TFLOP/s", "prefill TFLOP/s"
+        value, unit = world * fl / (ms * 1e-3) / 1e12, "TFLOP/s"
+        metric = "prefill TFLOP/s" if args.workload == "prefill" else "prefix-cached prefill TFLOP/s"
         ach = fl / (attn_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16"], "unit": "TFLOP/s",
                 "frac": ach / peaks["bf16"]}
@@ -521,7 +533,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["decode", "prefill", "mixed", "shared"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "prefill", "mixed", "shared", "prefix"],
+                    default="decode",
                     help="decode is the headline; the others print their own metric")
     ap.add_argument("--decode-seqs", type=int, default=0,
                     help="profile case: only the first N decode sequences, pool sized to fit")

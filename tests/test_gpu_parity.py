@@ -116,7 +116,7 @@ def _sample_rows(lay, rng, n_seq, rows_per_seq=3):
     return rows
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5, 6])
 def test_full_size_workload_sampled(cfg):
     lay = workloads.config_layout(cfg, 0)
     g = workloads.make_tensors(lay, seed=0, device=DEV, poison=True)
@@ -279,7 +279,7 @@ def test_prefill_kernels_match_oracle(lay, prefill_impl):
     H.assert_close(H.f64(out), H.oracle_full(lay, ts), f"{lay.name}/{prefill_impl}")
 
 
-@pytest.mark.parametrize("cfg", [3, 4])
+@pytest.mark.parametrize("cfg", [3, 4, 6])
 def test_prefill_full_size_both_kernels_agree(cfg, monkeypatch):
     # the tensor-core and the general kernel on the same full-size batch
     lay = workloads.config_layout(cfg, 0)

@@ -8,7 +8,7 @@ import workloads
 from oracle import blockmgr, metadata
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6])
 def test_generator_metadata_matches_oracle(cfg):
     lay = workloads.config_layout(cfg, 0)
     assert lay.query_start_loc.tolist() == metadata.query_start_loc(lay.query_lens).tolist()
@@ -48,6 +48,10 @@ def test_workload_shapes():
     s = workloads.config_layout(5)
     assert s.num_seqs == 64 and (s.query_lens == 1).all() and len(s.cow_pairs) == 63
     assert s.seq_lens.min() >= 16384 + 2 and s.seq_lens.max() <= 16384 + 257
+    x = workloads.config_layout(6)
+    assert x.num_seqs == 32 and x.num_decode_seqs == 0
+    assert x.cached_lens.min() >= 1024 and x.cached_lens.max() <= 8192
+    assert x.query_lens.min() >= 64 and x.query_lens.max() <= 512
 
 
 def test_shared_prefix_copy_pairs_follow_copy_on_write_rule():

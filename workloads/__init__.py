@@ -22,6 +22,10 @@ geometry, 32 heads of 128 dims, with ``max_num_seqs = 256`` and
 5. ``shared``  — 64 sequences sharing one 16384-token prompt (1024 blocks,
    ref count 64), private tails of uniform [1, 256] tokens, 1 decode token
    each; 63 copy-on-write pairs for the last prompt block; 64/8 heads.
+6. ``prefix``  — prefill on a cached prefix (a prefix-cache hit: only the
+   uncached suffix is computed, against the whole cached sequence): 32
+   sequences, cached history uniform in [1024, 8192], new chunks uniform in
+   [64, 512] tokens; 32/8 heads, head_dim 128, block_size 16.
 
 Placement: every sequence's logical blocks take consecutive entries of a
 seeded random permutation of the pool.  Values: N(0, 1) rounded to bf16.
@@ -34,7 +38,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-CONFIG_NAMES = {1: "worked", 2: "decode", 3: "prefill", 4: "mixed", 5: "shared"}
+CONFIG_NAMES = {1: "worked", 2: "decode", 3: "prefill", 4: "mixed", 5: "shared", 6: "prefix"}
 
 
 @dataclass
@@ -193,6 +197,10 @@ def config_layout(cfg: int, seed: int = 0) -> Layout:
         return custom_layout("mixed", cached, queries, 32, 8, 128, 16, 70_000, 4000 + seed)
     if cfg == 5:
         return shared_prefix_layout(seed)
+    if cfg == 6:
+        cached = rng.integers(1024, 8192, size=32, endpoint=True)
+        queries = rng.integers(64, 512, size=32, endpoint=True)
+        return custom_layout("prefix", cached, queries, 32, 8, 128, 16, 16_384, 6000 + seed)
     raise ValueError(f"no workload {cfg}")
 
 
