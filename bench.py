@@ -161,10 +161,11 @@ class ClockSampler:
 class Step:
     """Device-resident inputs of one workload and the calls of one step."""
 
-    def __init__(self, lay, dev, seed=0):
+    def __init__(self, lay, dev, seed=0, fused=False):
         import torch
         import paged_kv_cache_133_gb300 as pa
         self.pa, self.torch, self.lay, self.dev = pa, torch, lay, dev
+        self.fused = fused  # one pa_write_kv_attention call instead of pa_write_kv + pa_attention
         self.g = workloads.make_tensors(lay, seed=seed, device=dev)
         self.md = {
             "qsl": torch.from_numpy(lay.query_start_loc).to(dev),
@@ -185,6 +186,17 @@ class Step:
         md = md or self.md
         if len(lay.cow_pairs):
             pa.copy_blocks(g["k_cache"], g["v_cache"], md["pairs"], err=self.err)
+        if self.fused:
+            if attn_events is not None:
+                attn_events[0].record()
+            pa.write_kv_attention(g["q"], g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"],
+                                  md["qsl"], md["seq_lens"], md["bt"],
+                                  num_decode_seqs=lay.num_decode_seqs,
+                                  max_query_len=lay.max_query_len, max_seq_len=lay.max_seq_len,
+                                  scale=lay.scale, out=self.out, workspace=self.ws, err=self.err)
+            if attn_events is not None:
+                attn_events[1].record()
+            return
         pa.write_kv(g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"], err=self.err)
         if attn_events is not None:
             attn_events[0].record()
@@ -376,7 +388,11 @@ def secondary(dev, steps, warmup, peaks):
     ms, attn_ms, _ = time_device(st, steps, warmup, False)
     fl = attention_flops(lay, np.arange(lay.num_seqs))
     tf = fl / (attn_ms * 1e-3) / 1e12
+    del st
+    st = Step(lay, dev, fused=True)
+    msf, _, _ = time_device(st, steps, warmup, False)
     res["prefill"] = {"workload": "16 prompts (log-uniform 16..2048, sum 8192), 32q/8kv, D 128, bs 16",
+                      "fused_ms_per_step": msf, "fused_TFLOP/s_per_step": fl / (msf * 1e-3) / 1e12,
                       "metric": "prefill TFLOP/s", "value": tf, "ms_attention": attn_ms,
                       "ms_per_step": ms, "flops": fl,
                       "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16"],
@@ -387,7 +403,11 @@ def secondary(dev, steps, warmup, peaks):
     ms6, attn6, _ = time_device(st, steps, warmup, False)
     fl6 = attention_flops(lay, np.arange(lay.num_seqs))
     tf6 = fl6 / (attn6 * 1e-3) / 1e12
+    del st
+    st = Step(lay, dev, fused=True)
+    msf6, _, _ = time_device(st, steps, warmup, False)
     res["prefix"] = {"workload": "32 prefix-cache hits: cached U[1024,8192], new chunks U[64,512], 32q/8kv, D 128, bs 16",
+                     "fused_ms_per_step": msf6, "fused_TFLOP/s_per_step": fl6 / (msf6 * 1e-3) / 1e12,
                      "metric": "prefix-cached prefill TFLOP/s", "value": tf6, "ms_attention": attn6,
                      "ms_per_step": ms6, "flops": fl6,
                      "roofline": {"bound": "tensor", "achieved": tf6, "peak": peaks["bf16"],
@@ -401,6 +421,9 @@ def secondary(dev, steps, warmup, peaks):
     t_star = decode_kernel_bytes(lay, dec) / (peaks["hbm"] * 1e9) + \
         attention_flops(lay, pre) / (peaks["bf16"] * 1e12)
     del st
+    st = Step(lay, dev, fused=True)
+    ms4f, _, _ = time_device(st, steps, warmup, False)
+    del st
     lay5 = workloads.config_layout(5, 0)
     st = Step(lay5, dev)
     ms5, attn5, _ = time_device(st, steps, warmup, False)
@@ -411,7 +434,7 @@ def secondary(dev, steps, warmup, peaks):
                      "note": "the shared prefix (67 MB of K+V) stays in L2; logical bytes count it once per sequence"}
     res["mixed"] = {"workload": "240 decodes (history U[128,8192]) + 2 chunks of 3976 on 1024/3000 cached, 32q/8kv",
                     "metric": "mixed-batch attn tokens/s", "value": lay.num_tokens / (ms * 1e-3),
-                    "ms_per_step": ms, "ms_attention": attn_ms,
+                    "ms_per_step": ms, "ms_attention": attn_ms, "fused_ms_per_step": ms4f,
                     "additive_roofline_ms": t_star * 1e3, "frac": t_star * 1e3 / ms}
     del st
     res["swap"] = swap_leg(dev)
@@ -479,7 +502,7 @@ def run_other(args, dev, peaks, rank, world, dist_on):
     """One JSON line for the prefill, mixed or shared-prefix workload."""
     cfg = {"prefill": 3, "mixed": 4, "shared": 5, "prefix": 6}[args.workload]
     lay = workloads.config_layout(cfg, args.seed)
-    step = Step(lay, dev, seed=args.seed + rank)
+    step = Step(lay, dev, seed=args.seed + rank, fused=args.fused)
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     ms, attn_ms, launches = time_device(step, args.steps, args.warmup, dist_on, clocks)
     ms = _max_over_ranks(ms, dist_on, dev)
@@ -515,7 +538,7 @@ def run_other(args, dev, peaks, rank, world, dist_on):
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": lay.name, "ms_attention": attn_ms,
+            "config": {"workload": lay.name, "ms_attention": attn_ms, "fused": bool(args.fused),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roof, "cpu_baseline": None,
             "e2e": {"value": e2e_v, "unit": unit, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
@@ -533,6 +556,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="time pa_write_kv_attention instead of pa_write_kv + pa_attention")
     ap.add_argument("--workload", choices=["decode", "prefill", "mixed", "shared", "prefix"],
                     default="decode",
                     help="decode is the headline; the others print their own metric")
@@ -584,6 +609,10 @@ def main():
     traffic = measured_traffic("decode_kernel", "decode", digest)
     e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, dist_on)
     e2e_ms = _max_over_ranks(e2e_ms, dist_on, dev)
+    step.fused = True  # the same step through pa_write_kv_attention, for reference
+    fused_ms, _, _ = time_device(step, max(args.steps // 4, 1), args.warmup, dist_on)
+    fused_ms = _max_over_ranks(fused_ms, dist_on, dev)
+    step.fused = False
     sec = None
     if not args.no_secondary:
         del step
@@ -603,6 +632,7 @@ def main():
                                "head_dim 128, block_size 16, 70000-block pool (seed %d)" % args.seed,
                    "kv_bytes_per_step": kvb, "l2": "inputs larger than L2 (18 GB pool, 10 GB read per step)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
+                   "fused_ms_per_step": fused_ms,
                    "baseline_metric": BASELINE_METRIC},
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (+combine when split)",
                      "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",

@@ -129,6 +129,44 @@ int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_strid
                  size_t workspace_bytes, uint32_t* err_flag, void* stream);
 
 /*
+ * pa_write_kv_attention — pa_write_kv followed by pa_attention in one call,
+ * with the scatter folded into the attention kernels.  "vLLM 原理" §3.7 runs
+ * the two back to back in every forward (store_kvcache, then the attention
+ * call); "vLLM Continuous Batching：从 Forward Shape 理解两个核心参数"
+ * §2.3补充 defines slot_mapping as the slot that the block table gives to
+ * each new token's position.
+ *
+ * Arguments are those of pa_attention plus k, v ([num_tokens, num_kv_heads,
+ * head_dim] bf16, token strides k_stride_t / v_stride_t in elements, multiples
+ * of 8, 16-byte aligned) and slot_mapping ([num_tokens] int32, as in
+ * pa_write_kv).  k_cache / v_cache are written.
+ *
+ * Result: the caches are written exactly as pa_write_kv writes them, and out
+ * is the attention of pa_write_kv then pa_attention, provided that each new
+ * token's slot is the one its sequence's block table gives to its position.
+ *
+ * A step with no decode rows whose prefill runs on the tensor-core path is
+ * one launch: the kernel takes the K/V of positions c_s .. L_s - 1 from k, v
+ * rather than from the cache and stores each token's row into its slot.  It
+ * groups those new keys into 128-key tiles starting at c_s (the cached
+ * history keeps its tiles from position 0), so the result is bit-identical
+ * to the two calls for sequences without history and otherwise equal up to
+ * the order of the fp32 sums.  Any other step (decode rows present, block
+ * size below 8, or scale <= 0) scatters first and then attends, bit-identical
+ * to the two calls.
+ * Errors: as pa_write_kv and pa_attention.
+ */
+int pa_write_kv_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                          const void* k, int64_t k_stride_t, const void* v, int64_t v_stride_t,
+                          void* k_cache, void* v_cache, const int32_t* slot_mapping,
+                          const int32_t* query_start_loc, const int32_t* seq_lens,
+                          const int32_t* block_tables, int num_seqs, int num_tokens,
+                          int max_blocks_per_seq, int num_decode_seqs, int max_query_len,
+                          int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                          int block_size, int num_blocks, float scale, void* workspace,
+                          size_t workspace_bytes, uint32_t* err_flag, void* stream);
+
+/*
  * pa_copy_blocks — copy-on-write block copies, "vLLM 原理" §2.1: for each
  * pair (src, dst) in pairs (int32 [num_pairs, 2], device memory),
  * k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src], all

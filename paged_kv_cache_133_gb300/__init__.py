@@ -16,7 +16,8 @@ import ctypes
 import math
 import os
 
-__all__ = ["write_kv", "attention", "attention_noalloc", "copy_blocks", "swap_blocks", "workspace_size", "kernel_launches",
+__all__ = ["write_kv", "attention", "write_kv_attention", "attention_noalloc", "copy_blocks",
+           "swap_blocks", "workspace_size", "kernel_launches",
            "library_path", "load", "PaError", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN",
            "DEV_BAD_DECODE", "DEV_BAD_PAIR"]
 
@@ -43,6 +44,10 @@ _SIGNATURES = {
     "pa_attention": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i,
                             _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_f, _c_p,
                             _c_sz, _c_p, _c_p]),
+    "pa_write_kv_attention": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_i64, _c_p,
+                                     _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i,
+                                     _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_f, _c_p, _c_sz, _c_p,
+                                     _c_p]),
     "pa_copy_blocks": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_p, _c_p]),
     "pa_attention_noalloc": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i,
                                     _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
@@ -228,6 +233,51 @@ def attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, *, n
                              max_query_len, max_seq_len, hq, hkv, d, bs, nb, float(scale),
                              _ptr(workspace), wbytes, _ptr(err), _stream(stream))
     _check(rc, "pa_attention")
+    return out
+
+
+def write_kv_attention(q, k, v, k_cache, v_cache, slot_mapping, query_start_loc, seq_lens,
+                       block_tables, *, num_decode_seqs, max_query_len, max_seq_len, scale=None,
+                       out=None, workspace=None, err=None, stream=None):
+    """``write_kv`` then ``attention`` in one call, the scatter folded into the kernels.
+
+    Same result as the two calls in sequence when each new token's slot is the
+    one its sequence's block table gives to its position.
+    """
+    import torch
+    _bf16_rows(q, "q")
+    _bf16_rows(k, "k")
+    _bf16_rows(v, "v")
+    _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    for t, n in ((slot_mapping, "slot_mapping"), (query_start_loc, "query_start_loc"),
+                 (seq_lens, "seq_lens"), (block_tables, "block_tables")):
+        _i32(t, n)
+    _need(block_tables.dim() == 2, "block_tables must be [num_seqs, max_blocks_per_seq]")
+    nb, bs, hkv, d = k_cache.shape
+    T, hq, dq = q.shape
+    _need(dq == d and k.shape == (T, hkv, d) and v.shape == (T, hkv, d), "q / k / v shapes differ")
+    _need(slot_mapping.numel() == T, "slot_mapping must have one entry per token")
+    S = seq_lens.numel()
+    _need(query_start_loc.numel() == S + 1 and block_tables.shape[0] == S, "metadata sizes differ")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _bf16_rows(out, "out")
+        _need(out.shape == q.shape, "out shape differs from q")
+    need = workspace_size(num_decode_seqs, hq, hkv, d, max_seq_len)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().pa_write_kv_attention(
+        _ptr(out), out.stride(0), _ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(v), v.stride(0),
+        _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), _ptr(query_start_loc), _ptr(seq_lens),
+        _ptr(block_tables), S, T, block_tables.shape[1], num_decode_seqs, max_query_len,
+        max_seq_len, hq, hkv, d, bs, nb, float(scale), _ptr(workspace), wbytes, _ptr(err),
+        _stream(stream))
+    _check(rc, "pa_write_kv_attention")
     return out
 
 

@@ -31,9 +31,15 @@ int device_num_sms() {
 // Per-device side stream and fork/join events for running the decode rows
 // concurrently with the persistent prefill kernel.  Created once per device;
 // no device memory.
+// Streams for a mixed step: the prefill on `hi` (highest priority, so that
+// when both kernels become ready at once the block scheduler places the
+// persistent prefill CTAs first) and the decode on `lo`, both forked from and
+// joined back into the caller's stream.  Without the priority, back-to-back
+// steps sometimes let the decode grid fill every SM first and starve the
+// prefill (measured 1.22 against 0.92 ms on the mixed workload).
 struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t hi = nullptr, lo = nullptr;
+  cudaEvent_t fork = nullptr, join_hi = nullptr, join_lo = nullptr;
   bool ready = false;
 };
 static SideStream g_side[64];
@@ -44,9 +50,15 @@ static SideStream* side_stream() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   SideStream& s = g_side[dev];
   if (!s.ready) {
-    if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithPriority(&s.hi, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&s.lo, cudaStreamNonBlocking, least) != cudaSuccess)
+      return nullptr;
+    if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.join_hi, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.join_lo, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
     s.ready = true;
   }
   return &s;
@@ -208,13 +220,23 @@ size_t pa_attention_workspace_size(int num_decode_seqs, int num_q_heads, int num
                                              max_seq_len, &part, &nsplit);
 }
 
-int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
-                 const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
-                 const int32_t* seq_lens, const int32_t* block_tables, int num_seqs,
-                 int num_tokens, int max_blocks_per_seq, int num_decode_seqs, int max_query_len,
-                 int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
-                 int block_size, int num_blocks, float scale, void* workspace,
-                 size_t workspace_bytes, uint32_t* err_flag, void* stream) {
+// The new tokens' K/V and their slots, for the fused scatter + attention.
+struct FusedIn {
+  const void* k;
+  const void* v;
+  int64_t k_stride, v_stride;
+  const int32_t* slots;
+};
+
+static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                          const void* k_cache, const void* v_cache,
+                          const int32_t* query_start_loc, const int32_t* seq_lens,
+                          const int32_t* block_tables, int num_seqs, int num_tokens,
+                          int max_blocks_per_seq, int num_decode_seqs, int max_query_len,
+                          int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                          int block_size, int num_blocks, float scale, void* workspace,
+                          size_t workspace_bytes, uint32_t* err_flag, void* stream,
+                          const FusedIn* fused) {
   if (num_seqs < 0 || num_tokens < 0 || num_decode_seqs < 0 || num_decode_seqs > num_seqs ||
       max_query_len < 0 || max_seq_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq <= 0)
@@ -279,11 +301,34 @@ int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_strid
   }
   const bool has_decode = num_decode_seqs > 0 && max_seq_len > 0;
   const bool has_prefill = num_seqs > num_decode_seqs && max_query_len > 0;
+  if (fused) {
+    if (has_decode || (has_prefill && !prefill_tc_supported(a))) {
+      // Steps with decode rows (which run beside the prefill and read every
+      // key from the cache) and steps the general prefill kernel takes:
+      // scatter first, then attend.  Folding the scatter into a prefill that
+      // shares the GPU with an HBM-bound decode measured slower.
+      const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+      const int rc = cuda_status(launch_write_kv(fused->k, fused->v, fused->k_stride,
+                                                 fused->v_stride, const_cast<void*>(k_cache),
+                                                 const_cast<void*>(v_cache), fused->slots,
+                                                 num_tokens, num_blocks, block_size,
+                                                 static_cast<int>(row), err_flag, st));
+      if (rc != PA_OK) return rc;
+    } else if (has_prefill) {
+      // Prefill-only step on the tensor-core path: it reads the new tokens'
+      // K/V from k, v and stores them into their slots itself.
+      a.k_new = fused->k;
+      a.v_new = fused->v;
+      a.kn_stride = fused->k_stride;
+      a.vn_stride = fused->v_stride;
+      a.slots = fused->slots;
+    }
+  }
   // Mixed step: the decode rows are HBM-bound and the tensor-core prefill is
-  // bound by its own TMA stream, so they run side by side: the persistent
-  // prefill kernel takes all but mixed_decode_sms() SMs on the caller's
-  // stream and the decode launches on a side stream (fork/join with events,
-  // which CUDA graph capture also records).
+  // bound by its softmax and issue chain, so they run side by side: the
+  // persistent prefill kernel takes all but mixed_decode_sms() SMs on a
+  // high-priority side stream and the decode launches on a low-priority one
+  // (fork/join with events, which CUDA graph capture also records).
   const int reserve = has_decode && has_prefill && prefill_tc_supported(a)
                           ? mixed_decode_sms(device_num_sms())
                           : 0;
@@ -292,15 +337,18 @@ int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_strid
     SideStream* side = side_stream();
     if (side) {
       if (cudaEventRecord(side->fork, st) != cudaSuccess ||
-          cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+          cudaStreamWaitEvent(side->hi, side->fork, 0) != cudaSuccess ||
+          cudaStreamWaitEvent(side->lo, side->fork, 0) != cudaSuccess)
         return cuda_status(cudaGetLastError());
       a.max_ctas = device_num_sms() - reserve;
-      int rc = cuda_status(launch_prefill(a, st));
+      int rc = cuda_status(launch_prefill(a, side->hi));
       if (rc != PA_OK) return rc;
-      rc = cuda_status(launch_decode(a, side->stream));
+      rc = cuda_status(launch_decode(a, side->lo));
       if (rc != PA_OK) return rc;
-      if (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
-          cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
+      if (cudaEventRecord(side->join_hi, side->hi) != cudaSuccess ||
+          cudaEventRecord(side->join_lo, side->lo) != cudaSuccess ||
+          cudaStreamWaitEvent(st, side->join_hi, 0) != cudaSuccess ||
+          cudaStreamWaitEvent(st, side->join_lo, 0) != cudaSuccess)
         return cuda_status(cudaGetLastError());
       return PA_OK;
     }
@@ -314,6 +362,43 @@ int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_strid
     if (rc != PA_OK) return rc;
   }
   return PA_OK;
+}
+
+int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                 const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
+                 const int32_t* seq_lens, const int32_t* block_tables, int num_seqs,
+                 int num_tokens, int max_blocks_per_seq, int num_decode_seqs, int max_query_len,
+                 int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                 int block_size, int num_blocks, float scale, void* workspace,
+                 size_t workspace_bytes, uint32_t* err_flag, void* stream) {
+  return attention_impl(out, out_stride_t, q, q_stride_t, k_cache, v_cache, query_start_loc,
+                        seq_lens, block_tables, num_seqs, num_tokens, max_blocks_per_seq,
+                        num_decode_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
+                        head_dim, block_size, num_blocks, scale, workspace, workspace_bytes,
+                        err_flag, stream, nullptr);
+}
+
+int pa_write_kv_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                          const void* k, int64_t k_stride_t, const void* v, int64_t v_stride_t,
+                          void* k_cache, void* v_cache, const int32_t* slot_mapping,
+                          const int32_t* query_start_loc, const int32_t* seq_lens,
+                          const int32_t* block_tables, int num_seqs, int num_tokens,
+                          int max_blocks_per_seq, int num_decode_seqs, int max_query_len,
+                          int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                          int block_size, int num_blocks, float scale, void* workspace,
+                          size_t workspace_bytes, uint32_t* err_flag, void* stream) {
+  if (num_tokens > 0) {
+    if (!k || !v || !slot_mapping) return PA_ERR_INVALID_ARG;
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (k_stride_t < row || v_stride_t < row) return PA_ERR_INVALID_ARG;
+    if (k_stride_t % 8 || v_stride_t % 8 || !aligned16(k) || !aligned16(v)) return PA_ERR_UNSUPPORTED;
+  }
+  const FusedIn f{k, v, k_stride_t, v_stride_t, slot_mapping};
+  return attention_impl(out, out_stride_t, q, q_stride_t, k_cache, v_cache, query_start_loc,
+                        seq_lens, block_tables, num_seqs, num_tokens, max_blocks_per_seq,
+                        num_decode_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
+                        head_dim, block_size, num_blocks, scale, workspace, workspace_bytes,
+                        err_flag, stream, &f);
 }
 
 }  // extern "C"

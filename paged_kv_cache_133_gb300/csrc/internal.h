@@ -43,6 +43,14 @@ struct AttnArgs {
   unsigned int* sched;
   // cap on the persistent prefill grid (0: one CTA per SM)
   int max_ctas;
+  // Fused scatter for the prefill rows (null k_new: none).  The tensor-core
+  // prefill reads the new tokens' K/V from k_new / v_new ([T, Hkv, D], token
+  // strides in elements) for positions c_s .. L_s - 1 instead of from the
+  // cache, and stores each of those tokens' rows into its slot_mapping slot.
+  const void* k_new;
+  const void* v_new;
+  int64_t kn_stride, vn_stride;
+  const int32_t* slots;
 };
 
 // Bytes at the start of the workspace reserved for the prefill work queue.

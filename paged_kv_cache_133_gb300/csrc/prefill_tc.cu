@@ -145,11 +145,29 @@ constexpr int kRingOffset = 8 * 32;  // bytes after the barriers (TMEM slot + fl
 
 struct Item {
   int s, hk, h[2], t0, qn, c, i0, kv_end, n;  // h[1] < 0: no second tile
+  int nh;  // fused scatter: tiles of cached history before the new-token tiles (else 0)
 };
+
+// Key range [key0, key_end) of tile j of an item.  Without the fused scatter
+// the tiles are 128-position windows from position 0.  With it, the cached
+// history c comes first in 128-position windows (the last one cut at c),
+// then the new tokens in 128-position windows starting at c, so that every
+// new-token tile is 128 consecutive input rows.
+__device__ __forceinline__ void tile_keys(const Item& I, int j, bool fused, int& key0,
+                                          int& key_end) {
+  if (fused && j >= I.nh) {
+    key0 = I.c + (j - I.nh) * kN;
+    key_end = min(key0 + kN, I.kv_end);
+  } else {
+    key0 = j * kN;
+    key_end = min(key0 + kN, fused ? I.c : I.kv_end);
+  }
+}
 
 // Work slot e -> item.  Slots enumerate (cost level from max_level down to 1,
 // sequence, kv head, head pair); the sequence's tile at that level is
 // t = level - 1 - ceil(c / 128); a slot whose tile does not exist is empty.
+template <bool kFused>
 __device__ bool decode_item(const AttnArgs& a, int e, int pairs, int max_level, Item& it,
                             bool& bad) {
   const int S_pre = a.num_seqs - a.num_decode;
@@ -184,16 +202,24 @@ __device__ bool decode_item(const AttnArgs& a, int e, int pairs, int max_level, 
   it.c = L - qn;
   it.i0 = tile * kM;
   it.kv_end = it.c + min(qn, it.i0 + kM);
-  it.n = (it.kv_end + kN - 1) / kN;
+  if (kFused) {
+    it.nh = (it.c + kN - 1) / kN;
+    it.n = it.nh + it.i0 / kN + 1;
+  } else {
+    it.nh = 0;
+    it.n = (it.kv_end + kN - 1) / kN;
+  }
   return true;
 }
 
-template <int D>
+template <int D, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_o, const AttnArgs a,
+                      const __grid_constant__ CUtensorMap tm_o,
+                      const __grid_constant__ CUtensorMap tm_kn,
+                      const __grid_constant__ CUtensorMap tm_vn, const AttnArgs a,
                       int total_slots, int max_level) {
   using Ly = PpLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -228,6 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_o);
+    if (kFused) {
+      prefetch_tmap(&tm_kn);
+      prefetch_tmap(&tm_vn);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -269,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int e = static_cast<int>(atomicAdd(a.sched, 1u));
           if (e >= total_slots) break;
           bool bad;
-          if (decode_item(a, e, pairs, max_level, I, bad)) break;
+          if (decode_item<kFused>(a, e, pairs, max_level, I, bad)) break;
           if (bad) flag_error(a.err, PA_DEV_BAD_LEN);
         }
         const int slot = it & 1;
@@ -298,16 +328,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kProducerWarp || warp == kVWarp) {
     // ------------------------------------------------------------ producers
-    // warp 8: the K tiles; warp 10: the V tiles.
+    // warp 8: the K tiles; warp 10: the V tiles.  Cached positions come from
+    // the paged cache, one TMA box per block (lane b issues box b).  With the
+    // fused scatter, the new tokens' tiles (see tile_keys) are 128
+    // consecutive rows of the new-token K/V: one box per 64-column half.
+    // Items of the first head pair then store their own query rows' K (V)
+    // into their slots, read back from the item's last tile in shared memory.
     const bool is_k = warp == kProducerWarp;
     const int nst = is_k ? Ly::kKStages : Ly::kVStages;
     const int full0 = is_k ? bKFull0 : bVFull0;
     const int empty0 = is_k ? bKEmpty0 : bVEmpty0;
     const uint32_t stage0 = base + (is_k ? Ly::kK : Ly::kV);
     const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+    const CUtensorMap* nmap = is_k ? &tm_kn : &tm_vn;
+    constexpr bool fused = kFused;
+    constexpr int kCpr = D / 8;  // 16-byte pieces per row
+    int gt = 0, it = 0, last = -1;
+    // Pending store of an item's own rows (fused scatter): the tile holding
+    // them and the item.  Lane r stores rows r, r + 32, ... (one slot each,
+    // 16-byte pieces in order), which keeps the instruction count low: this
+    // warp shares its sub-partition with two softmax warps.  The store runs
+    // while this warp would otherwise wait for a free stage, and at the
+    // latest before that tile's stage is refilled.
+    int pend_g = -1;
+    Item pend_I{};
+    auto scatter = [&]() -> bool {
+      const int g = pend_g;
+      if (!wait(full0 + g % nst, g / nst)) return false;
+      const uint8_t* sg = sgen + (stage0 - base) + (g % nst) * Ly::kTile;
+      const Item& P = pend_I;
+      const int rows = min(kM, P.qn - P.i0);
+      const int64_t nslots = static_cast<int64_t>(a.num_blocks) << a.bs_log2;
+      __nv_bfloat16* cw = static_cast<__nv_bfloat16*>(const_cast<void*>(is_k ? a.k_cache : a.v_cache)) +
+                          static_cast<int64_t>(P.hk) * D;
+#pragma unroll 1
+      for (int r = lane; r < rows; r += 32) {
+        const int sl = __ldg(a.slots + P.t0 + P.i0 + r);
+        if (sl >= nslots) {
+          flag_error(a.err, PA_DEV_BAD_SLOT);
+        } else if (sl >= 0) {
+          uint4* dst = reinterpret_cast<uint4*>(cw + static_cast<int64_t>(sl) * a.hkv * D);
+          const uint8_t* src = sg + r * 128;
+#pragma unroll
+          for (int c16 = 0; c16 < kCpr; ++c16)
+            dst[c16] = *reinterpret_cast<const uint4*>(src + (c16 >> 3) * Ly::kHalf +
+                                                        (((c16 & 7) ^ (r & 7)) << 4));
+        }
+      }
+      __syncwarp();
+      pend_g = -1;
+      return true;
+    };
+    // Before waiting for stage st of tile gt.
+    auto before_refill = [&](int st) -> bool {
+      if (pend_g < 0) return true;
+      if (st != pend_g % nst) {  // optional: only while the stage is busy and the rows are in
+        const bool busy = gt >= nst && !__all_sync(0xffffffffu, mbar_try_wait(BAR(empty0 + st),
+                                                                              (gt / nst - 1) & 1));
+        const bool landed = __all_sync(0xffffffffu, mbar_try_wait(BAR(full0 + pend_g % nst),
+                                                                  (pend_g / nst) & 1));
+        if (!busy || !landed) return true;
+      }
+      return scatter();
+    };
     const int bs = 1 << a.bs_log2;
     const int R = bs < kN ? bs : kN;  // cache rows per TMA box; lane b owns box b
-    int gt = 0, it = 0, last = -1;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       Item I;
@@ -316,32 +401,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(BAR(bItemEmpty0 + (k & 1)));
       ++it;
       const int32_t* bt = a.block_tables + static_cast<int64_t>(I.s) * a.max_blocks;
+      const int64_t head = static_cast<int64_t>(I.hk) * D;
       for (int j = 0; j < I.n; ++j, ++gt) {
         const int st = gt % nst;
-        const int p0 = j * kN;
-        const int nbox = (min(I.kv_end, p0 + kN) - p0 + R - 1) / R;
+        int key0, key_end;
+        tile_keys(I, j, fused, key0, key_end);
+        const uint32_t stile = stage0 + st * Ly::kTile;
+        if (fused && j >= I.nh) {
+          // new tokens: input rows t0 + (key0 - c) ..., one 128-row box per half
+          if (!(ok = before_refill(st))) break;
+          if (gt >= nst && !(ok = wait(empty0 + st, gt / nst - 1))) break;
+          if (lane == 0) {
+            mbar_expect_tx(BAR(full0 + st), kN * 128 * Ly::kHalves);
+#pragma unroll
+            for (int hf = 0; hf < Ly::kHalves; ++hf)
+              tma_load_2d(stile + hf * Ly::kHalf, nmap, static_cast<int>(head) + hf * 64,
+                          I.t0 + (key0 - I.c), BAR(full0 + st));
+          }
+          __syncwarp();
+          last = gt;
+          continue;
+        }
+        // cached positions: one box per block
+        const int nbox = (key_end - key0 + R - 1) / R;
         int slot = -1;
         const int b = lane;
         if (b < nbox) {
-          const int pos = p0 + b * R;
+          const int pos = key0 + b * R;
           const int pb = __ldg(bt + (pos >> a.bs_log2));
           if (pb >= 0 && pb < a.num_blocks) slot = (pb << a.bs_log2) + (pos & (bs - 1));
           else flag_error(a.err, PA_DEV_BAD_BLOCK);
         }
         const uint32_t valid = __ballot_sync(0xffffffffu, slot >= 0);
         const uint32_t bytes = static_cast<uint32_t>(__popc(valid) * R * 128 * Ly::kHalves);
+        if (!(ok = before_refill(st))) break;
         if (gt >= nst && !(ok = wait(empty0 + st, gt / nst - 1))) break;
         if (lane == 0) mbar_expect_tx(BAR(full0 + st), bytes);
         __syncwarp();
         if (slot >= 0) {
-          const uint32_t dst = stage0 + st * Ly::kTile + b * R * 128;
+          const uint32_t dst = stile + b * R * 128;
 #pragma unroll
           for (int hf = 0; hf < Ly::kHalves; ++hf)
             tma_load_3d(dst + hf * Ly::kHalf, map, hf * 64, I.hk, slot, BAR(full0 + st));
         }
         last = gt;
       }
+      if (!ok) break;
+      if (fused && I.h[0] == I.hk * a.group) {
+        // The item's last tile holds its own query rows' K (V) as rows
+        // 0 .. rows - 1: store them into their slots once it has landed.
+        if (pend_g >= 0 && !(ok = scatter())) break;
+        pend_g = gt - 1;
+        pend_I = I;
+      }
     }
+    if (ok && pend_g >= 0) ok = scatter();
     // drain: every copy this warp issued has landed before the CTA exits
     if (lane == 0) {
       for (int t = max(0, last - nst + 1); t <= last; ++t)
@@ -456,8 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the P columns and O may be rewritten below.
         if (!(ok = wait(side ? bSB : bSA, gx + j))) break;
         tc_fence_after();
-        const int key0 = j * kN;
-        const bool full = key0 + kN - 1 <= lim && key0 + kN <= I.kv_end;
+        int key0, key_end;
+        tile_keys(I, j, kFused, key0, key_end);
+        const bool full = key0 + kN - 1 <= lim && key0 + kN <= key_end;
         uint32_t sr[128];
         tmem_ld128(tS, sr);
         tmem_wait_ld();
@@ -465,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // scaling); masked keys become -inf.
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (!full) {
-          const int last = min(lim, I.kv_end - 1) - key0;  // last visible column of this row
+          const int last = min(lim, key_end - 1) - key0;  // last visible column of this row
 #pragma unroll
           for (int e2 = 0; e2 < 128; ++e2)
             if (e2 > last) sr[e2] = __float_as_uint(-INFINITY);
@@ -514,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         m_used = m_new;
-        const int live = I.kv_end - key0;  // rows [live, 128) of V_j are not keys
+        const int live = key_end - key0;  // rows [live, 128) of V_j are not keys
         if (side == 0 && live < kN) {
           if (!(ok = wait(bVFull0 + (gx + j) % Ly::kVStages, (gx + j) / Ly::kVStages))) break;
           uint8_t* vt = sgen + Ly::kV + ((gx + j) % Ly::kVStages) * Ly::kTile;
@@ -667,6 +782,20 @@ bool encode_out(CUtensorMap* m, const AttnArgs& a) {
            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The new tokens' K or V ([T, Hkv, D], token stride in elements): 128-row boxes.
+bool encode_new(CUtensorMap* m, const void* ptr, int64_t stride, const AttnArgs& a) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.hkv) * a.head_dim,
+                              static_cast<cuuint64_t>(a.num_tokens)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride) * 2};
+  const cuuint32_t box[2] = {64, kN};
+  const cuuint32_t es[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Highest cost level: every visible key range is at most max_seq_len keys.
 int max_level_of(const AttnArgs& a) { return (a.max_seq_len + kN - 1) / kN + 1; }
 
@@ -675,21 +804,25 @@ int64_t total_slots_of(const AttnArgs& a) {
   return static_cast<int64_t>(a.hkv) * pairs * (a.num_seqs - a.num_decode) * max_level_of(a);
 }
 
-template <int D>
+template <int D, bool kFused>
 cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   using Ly = PpLayout<D>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mkn, mvn;
+  memset(&mkn, 0, sizeof(mkn));  // unused without the fused scatter
+  memset(&mvn, 0, sizeof(mvn));
   if (!encode_q(&mq, a) || !encode_cache(&mk, a.k_cache, a) || !encode_cache(&mv, a.v_cache, a) ||
-      !encode_out(&mo, a))
+      !encode_out(&mo, a) ||
+      (a.k_new && (!encode_new(&mkn, a.k_new, a.kn_stride, a) ||
+                   !encode_new(&mvn, a.v_new, a.vn_stride, a))))
     return cudaErrorNotSupported;  // nothing launched: the caller takes the general kernel
   const int total = static_cast<int>(total_slots_of(a));
   int sms = device_num_sms();
@@ -699,7 +832,8 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
   if (e != cudaSuccess) return e;
   count_launch();
-  prefill_tc_kernel<D><<<grid, kThreads, Ly::kAlloc, st>>>(mq, mk, mv, mo, a, total, max_level_of(a));
+  prefill_tc_kernel<D, kFused><<<grid, kThreads, Ly::kAlloc, st>>>(mq, mk, mv, mo, mkn, mvn, a, total,
+                                                            max_level_of(a));
   return cudaGetLastError();
 }
 
@@ -721,7 +855,8 @@ bool prefill_tc_supported(const AttnArgs& a) {
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t st) {
   if (a.num_seqs - a.num_decode <= 0 || a.max_query_len <= 0) return cudaSuccess;
-  return a.head_dim == 128 ? launch_tc_d<128>(a, st) : launch_tc_d<64>(a, st);
+  if (a.k_new) return a.head_dim == 128 ? launch_tc_d<128, true>(a, st) : launch_tc_d<64, true>(a, st);
+  return a.head_dim == 128 ? launch_tc_d<128, false>(a, st) : launch_tc_d<64, false>(a, st);
 }
 
 }  // namespace pa
