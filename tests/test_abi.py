@@ -38,7 +38,7 @@ def lib():
 def test_header_declares_the_three_calls():
     names = _declared()
     for n in ("pa_write_kv", "pa_attention", "pa_attention_workspace_size", "pa_copy_blocks",
-              "pa_swap_blocks"):
+              "pa_swap_blocks", "pa_write_kv_attention"):
         assert n in names
 
 
@@ -98,3 +98,15 @@ def test_swap_binding_refuses_pageable_host_pools():
     t = torch.zeros((2, 1, 1, 8), dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="pinned"):
         pa.swap_blocks(t, t, t, t, None)
+
+
+def test_fused_call_validates_its_extra_arguments(lib):
+    nul = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    args = lambda k, ks, slots: (fake, 512, fake, 512, k, ks, fake, ks, fake, fake, slots, fake,
+                                 fake, fake, 1, 4, 1, 0, 4, 4, 4, 1, 128, 16, 8, 1.0, fake,
+                                 1 << 20, nul, nul)
+    assert lib.pa_write_kv_attention(*args(nul, 128, fake)) == 1   # no k
+    assert lib.pa_write_kv_attention(*args(fake, 128, nul)) == 1   # no slot_mapping
+    assert lib.pa_write_kv_attention(*args(fake, 64, fake)) == 1   # token stride < Hkv * D
+    assert lib.pa_write_kv_attention(*args(fake, 132, fake)) == 2  # stride not a multiple of 8
