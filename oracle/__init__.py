@@ -27,6 +27,8 @@ Modules:
 * ``brute``     — the same attention with scalar Python loops (tiny inputs only).
 * ``padded``    — the ``[S, L_max]`` + attention-mask formulation.
 * ``blockmgr``  — a test-only block allocator with ref counts and copy-on-write.
+* ``fp8``       — the 8-bit (E4M3) cache encoding: quantise, dequantise, scatter
+  (an extension; the pages' cache is bf16).
 
 Every function here is pinned by ``tests/test_oracle_*.py`` to something other
 than itself: the pages' worked integers, closed forms, a library routine it
