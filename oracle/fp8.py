@@ -47,28 +47,21 @@ _POS_VALUES = _VALUES[_POS_CODES]
 def e4m3_encode(y) -> np.ndarray:
     """Nearest E4M3 code of each value (ties to the even code, saturating)."""
     y = np.asarray(y, dtype=np.float64)
-    flat = y.reshape(-1)
-    codes = np.empty(flat.shape, dtype=np.uint8)
-    for i, v in enumerate(flat.tolist()):
-        if v != v:
-            codes[i] = NAN_CODE
-            continue
-        sign = 0x80 if (v < 0 or (v == 0 and np.signbit(v))) else 0
-        a = min(abs(v), MAX_FINITE)
-        j = int(np.searchsorted(_POS_VALUES, a))     # first value >= a
-        if j < len(_POS_VALUES) and _POS_VALUES[j] == a:
-            c = j
-        else:
-            lo, hi = j - 1, j                         # a lies strictly between them
-            d_lo, d_hi = a - _POS_VALUES[lo], _POS_VALUES[hi] - a
-            if d_lo < d_hi:
-                c = lo
-            elif d_hi < d_lo:
-                c = hi
-            else:
-                c = lo if lo % 2 == 0 else hi
-        codes[i] = sign | int(_POS_CODES[c])
-    return codes.reshape(y.shape)
+    a = np.minimum(np.abs(y), MAX_FINITE)
+    nan = np.isnan(y)
+    a = np.where(nan, 0.0, a)
+    j = np.searchsorted(_POS_VALUES, a)                 # first value >= a
+    j_c = np.minimum(j, len(_POS_VALUES) - 1)
+    exact = _POS_VALUES[j_c] == a
+    lo = np.maximum(j - 1, 0)
+    hi = j_c
+    d_lo = a - _POS_VALUES[lo]
+    d_hi = _POS_VALUES[hi] - a
+    pick = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    c = np.where(exact, j_c, pick)
+    sign = np.where(np.signbit(y), 0x80, 0)
+    codes = (sign | _POS_CODES[c]).astype(np.uint8)
+    return np.where(nan, NAN_CODE, codes).astype(np.uint8)
 
 
 def quantize(x, scale: float) -> np.ndarray:
