@@ -206,6 +206,43 @@ int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_
                    void* stream);
 
 /*
+ * 8-bit KV cache (an extension: the pages' cache is bf16).  The cache holds
+ * OCP E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, largest finite magnitude 448) with one scale per tensor:
+ * value = code * scale.  Same [num_blocks, block_size, num_kv_heads,
+ * head_dim] layout, one byte per element, 16-byte aligned.
+ *
+ * pa_write_kv_fp8 — pa_write_kv into an 8-bit cache: each element x of the
+ * new rows is stored as the E4M3 code nearest to fp32(x) * fp32(1 / scale)
+ * (ties to the even code, magnitudes past 448 clamped to 448).  Scales must
+ * be positive and finite (PA_ERR_INVALID_ARG); num_kv_heads * head_dim must
+ * be a multiple of 16 and the token strides multiples of 8 elements
+ * (PA_ERR_UNSUPPORTED).  Device errors as pa_write_kv.
+ */
+int pa_write_kv_fp8(const void* k, const void* v, int64_t k_stride_t, int64_t v_stride_t,
+                    void* k_cache, void* v_cache, const int32_t* slot_mapping, int num_tokens,
+                    int num_blocks, int block_size, int num_kv_heads, int head_dim, float k_scale,
+                    float v_scale, uint32_t* err_flag, void* stream);
+
+/*
+ * pa_attention_fp8 — pa_attention over an 8-bit cache, for decode steps:
+ * every sequence must be a decode row (num_decode_seqs == num_seqs, else
+ * PA_ERR_UNSUPPORTED; the tensor-core prefill reads bf16 only).  Keys and
+ * values are the codes times k_scale / v_scale.  The kernel widens each
+ * 16-token group to fp16 (exact for every code) and runs the products in
+ * fp16 with fp32 accumulation; q is converted to fp16 once, so |q| must stay
+ * below 65504.  Workspace and errors as pa_attention.
+ */
+int pa_attention_fp8(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                     const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
+                     const int32_t* seq_lens, const int32_t* block_tables, int num_seqs,
+                     int num_tokens, int max_blocks_per_seq, int num_decode_seqs,
+                     int max_query_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int num_blocks, float scale, float k_scale,
+                     float v_scale, void* workspace, size_t workspace_bytes, uint32_t* err_flag,
+                     void* stream);
+
+/*
  * pa_attention_noalloc — pa_attention without a workspace argument, for
  * callers that cannot allocate device memory (a library embedded in a host
  * application that owns every device allocation, a runtime whose memory is

@@ -17,7 +17,7 @@ import math
 import os
 
 __all__ = ["write_kv", "attention", "write_kv_attention", "attention_noalloc", "copy_blocks",
-           "swap_blocks", "workspace_size", "kernel_launches",
+           "swap_blocks", "write_kv_fp8", "attention_fp8", "workspace_size", "kernel_launches",
            "library_path", "load", "PaError", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN",
            "DEV_BAD_DECODE", "DEV_BAD_PAIR"]
 
@@ -48,6 +48,11 @@ _SIGNATURES = {
                                      _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i,
                                      _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_f, _c_p, _c_sz, _c_p,
                                      _c_p]),
+    "pa_write_kv_fp8": (_c_i, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i,
+                               _c_i, _c_f, _c_f, _c_p, _c_p]),
+    "pa_attention_fp8": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i,
+                                _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_f, _c_f,
+                                _c_f, _c_p, _c_sz, _c_p, _c_p]),
     "pa_copy_blocks": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_p, _c_p]),
     "pa_attention_noalloc": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i,
                                     _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
@@ -130,6 +135,13 @@ def _cache(t, name):
           f"{name} must be a contiguous bf16 CUDA tensor [num_blocks, block_size, kv_heads, head_dim]")
 
 
+def _cache8(t, name):
+    import torch
+    _need(t.element_size() == 1 and t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
+          and t.is_cuda and t.is_contiguous() and t.dim() == 4,
+          f"{name} must be a contiguous 8-bit CUDA tensor [num_blocks, block_size, kv_heads, head_dim]")
+
+
 def kernel_launches() -> int:
     return int(load().pa_kernel_launches())
 
@@ -149,6 +161,57 @@ def write_kv(k, v, k_cache, v_cache, slot_mapping, err=None, stream=None):
     rc = load().pa_write_kv(_ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(k_cache), _ptr(v_cache),
                             _ptr(slot_mapping), T, nb, bs, hkv, d, _ptr(err), _stream(stream))
     _check(rc, "pa_write_kv")
+
+
+def write_kv_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale, err=None, stream=None):
+    """Scatter new-token K/V rows into an 8-bit (E4M3) cache: codes of x / scale."""
+    _bf16_rows(k, "k")
+    _bf16_rows(v, "v")
+    _cache8(k_cache, "k_cache")
+    _cache8(v_cache, "v_cache")
+    _i32(slot_mapping, "slot_mapping")
+    nb, bs, hkv, d = k_cache.shape
+    _need(tuple(v_cache.shape) == (nb, bs, hkv, d), "k_cache and v_cache shapes differ")
+    _need(k.shape[1:] == (hkv, d) and v.shape[1:] == (hkv, d), "k/v head shape mismatch")
+    T = slot_mapping.numel()
+    _need(k.shape[0] >= T and v.shape[0] >= T, "k/v have fewer rows than slot_mapping")
+    rc = load().pa_write_kv_fp8(_ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(slot_mapping), T, nb, bs, hkv, d,
+                                float(k_scale), float(v_scale), _ptr(err), _stream(stream))
+    _check(rc, "pa_write_kv_fp8")
+
+
+def attention_fp8(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, *, k_scale,
+                  v_scale, max_seq_len, scale=None, out=None, workspace=None, err=None,
+                  stream=None):
+    """Decode attention over an 8-bit (E4M3) cache; every sequence is a decode row."""
+    import torch
+    _bf16_rows(q, "q")
+    _cache8(k_cache, "k_cache")
+    _cache8(v_cache, "v_cache")
+    for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
+                 (block_tables, "block_tables")):
+        _i32(t, n)
+    nb, bs, hkv, d = k_cache.shape
+    T, hq, dq = q.shape
+    _need(dq == d, "q head_dim differs from the cache's")
+    S = seq_lens.numel()
+    _need(query_start_loc.numel() == S + 1 and block_tables.shape[0] == S, "metadata sizes differ")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    need = workspace_size(S, hq, hkv, d, max_seq_len)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().pa_attention_fp8(_ptr(out), out.stride(0), _ptr(q), q.stride(0), _ptr(k_cache),
+                                 _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens),
+                                 _ptr(block_tables), S, T, block_tables.shape[1], S, 1,
+                                 max_seq_len, hq, hkv, d, bs, nb, float(scale), float(k_scale),
+                                 float(v_scale), _ptr(workspace), wbytes, _ptr(err), _stream(stream))
+    _check(rc, "pa_attention_fp8")
+    return out
 
 
 def copy_blocks(k_cache, v_cache, pairs, err=None, stream=None):

@@ -236,7 +236,7 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
                           int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
                           int block_size, int num_blocks, float scale, void* workspace,
                           size_t workspace_bytes, uint32_t* err_flag, void* stream,
-                          const FusedIn* fused) {
+                          const FusedIn* fused, const float* kv_scales = nullptr) {
   if (num_seqs < 0 || num_tokens < 0 || num_decode_seqs < 0 || num_decode_seqs > num_seqs ||
       max_query_len < 0 || max_seq_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq <= 0)
@@ -262,6 +262,7 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
     return PA_ERR_UNSUPPORTED;
 
   AttnArgs a{};
+  a.inv_v_scale = 1.f;
   a.out = out;
   a.out_stride = out_stride_t;
   a.q = q;
@@ -301,6 +302,12 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
   }
   const bool has_decode = num_decode_seqs > 0 && max_seq_len > 0;
   const bool has_prefill = num_seqs > num_decode_seqs && max_query_len > 0;
+  if (kv_scales) {  // 8-bit cache: decode rows only
+    if (has_prefill) return PA_ERR_UNSUPPORTED;
+    a.kv_fp8 = true;
+    a.scale_log2 *= kv_scales[0];
+    a.inv_v_scale = 1.f / kv_scales[1];
+  }
   if (fused) {
     if (has_decode || (has_prefill && !prefill_tc_supported(a))) {
       // Steps with decode rows (which run beside the prefill and read every
@@ -399,6 +406,47 @@ int pa_write_kv_attention(void* out, int64_t out_stride_t, const void* q, int64_
                         num_decode_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
                         head_dim, block_size, num_blocks, scale, workspace, workspace_bytes,
                         err_flag, stream, &f);
+}
+
+int pa_write_kv_fp8(const void* k, const void* v, int64_t k_stride_t, int64_t v_stride_t,
+                    void* k_cache, void* v_cache, const int32_t* slot_mapping, int num_tokens,
+                    int num_blocks, int block_size, int num_kv_heads, int head_dim, float k_scale,
+                    float v_scale, uint32_t* err_flag, void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale))
+    return PA_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping) return PA_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row % 16 || k_stride_t % 8 || v_stride_t % 8 || k_stride_t < row || v_stride_t < row)
+    return PA_ERR_UNSUPPORTED;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_UNSUPPORTED;
+  return cuda_status(launch_write_kv_fp8(k, v, k_stride_t, v_stride_t, k_cache, v_cache,
+                                         slot_mapping, num_tokens, num_blocks, block_size,
+                                         static_cast<int>(row), 1.f / k_scale, 1.f / v_scale,
+                                         err_flag, static_cast<cudaStream_t>(stream)));
+}
+
+int pa_attention_fp8(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                     const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
+                     const int32_t* seq_lens, const int32_t* block_tables, int num_seqs,
+                     int num_tokens, int max_blocks_per_seq, int num_decode_seqs,
+                     int max_query_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int num_blocks, float scale, float k_scale,
+                     float v_scale, void* workspace, size_t workspace_bytes, uint32_t* err_flag,
+                     void* stream) {
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale))
+    return PA_ERR_INVALID_ARG;
+  const float scales[2] = {k_scale, v_scale};
+  return attention_impl(out, out_stride_t, q, q_stride_t, k_cache, v_cache, query_start_loc,
+                        seq_lens, block_tables, num_seqs, num_tokens, max_blocks_per_seq,
+                        num_decode_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
+                        head_dim, block_size, num_blocks, scale, workspace, workspace_bytes,
+                        err_flag, stream, nullptr, scales);
 }
 
 }  // extern "C"

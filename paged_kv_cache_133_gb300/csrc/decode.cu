@@ -32,21 +32,28 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kGrp = 16;  // tokens per warp step
 
-template <int D, int STAGES>
+// kFp8: the cache holds E4M3 codes.  The ring then stages the 8-bit rows
+// (plain layout), and each group is widened to fp16 (exact for every E4M3
+// value) into one swizzled K/V tile pair per warp before the products, which
+// then run as fp16 mma.sync with the query converted to fp16 once.
+template <int D, int STAGES, bool kFp8>
 struct DecLayout {
   static constexpr int kRow = D * 2;         // bytes of one token's K (or V) for one head
-  static constexpr int kTile = kGrp * kRow;  // K or V of one group
-  static constexpr int kStage = 2 * kTile;
-  static constexpr int kWarp = STAGES * kStage;
+  static constexpr int kTile = kGrp * kRow;  // K or V of one group (16-bit)
+  static constexpr int kRow8 = D;            // 8-bit row
+  static constexpr int kTile8 = kGrp * kRow8;
+  static constexpr int kStage = kFp8 ? 2 * kTile8 : 2 * kTile;
+  static constexpr int kConv = kFp8 ? 2 * kTile : 0;  // widened K/V of the current group
+  static constexpr int kWarp = STAGES * kStage + kConv;
   static constexpr int kLoop = kWarps * kWarp;
   static constexpr int kMergeFloats = 32 + 16 * D;  // m[16], l[16], acc[16][D]
   static constexpr int kMerge = kWarps * kMergeFloats * 4;
   static constexpr int kBytes = kLoop > kMerge ? kLoop : kMerge;
 };
 
-template <int D, int STAGES>
+template <int D, int STAGES, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
-  using Ly = DecLayout<D, STAGES>;
+  using Ly = DecLayout<D, STAGES, kFp8>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x;
   const int nhc = (a.group + 15) >> 4;
@@ -93,6 +100,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
       qa[ks][2] = va ? __ldg(pa_ + ks * 8 + 4) : 0u;
       qa[ks][3] = vb ? __ldg(pb_ + ks * 8 + 4) : 0u;
     }
+    if (kFp8) {  // bf16 -> fp16 pairs (exact in range for attention inputs)
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&qa[ks][j]);
+          qa[ks][j] = pack_f16(__low2float(b), __high2float(b));
+        }
+    }
   }
 
   const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.k_cache);
@@ -121,6 +137,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
       }
     }
     const uint32_t kdst = wbase + stage * Ly::kStage;
+    if (kFp8) {
+      const uint32_t vdst = kdst + Ly::kTile8;
+      const uint8_t* kc8 = static_cast<const uint8_t*>(a.k_cache);
+      const uint8_t* vc8 = static_cast<const uint8_t*>(a.v_cache);
+      constexpr int CPR8 = D / 16;  // 16-byte pieces per 8-bit row
+#pragma unroll
+      for (int i = 0; i < kGrp * CPR8 / 32; ++i) {
+        const int idx = i * 32 + lane;
+        const int r = idx / CPR8, c = idx % CPR8;
+        const int slot = __shfl_sync(0xffffffffu, my_slot, r);
+        const bool ok = slot >= 0;
+        const int64_t off = ok ? static_cast<int64_t>(slot) * slot_stride + head_off + c * 16 : 0;
+        cp_async16(kdst + r * Ly::kRow8 + c * 16, kc8 + off, ok);
+        cp_async16(vdst + r * Ly::kRow8 + c * 16, vc8 + off, ok);
+      }
+      return;
+    }
     const uint32_t vdst = kdst + Ly::kTile;
     constexpr int CPR = D / 8;  // 16-byte pieces per row
 #pragma unroll
@@ -156,8 +189,41 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
     cp_async_wait<STAGES - 1>();
     __syncwarp();
     const int st = k % STAGES;
-    const uint32_t kb = wbase + st * Ly::kStage;
-    const uint32_t vb = kb + Ly::kTile;
+    uint32_t kb = wbase + st * Ly::kStage;
+    uint32_t vb = kb + Ly::kTile;
+    if (kFp8) {
+      // widen the staged 8-bit rows into this warp's fp16 tiles (same
+      // swizzle as the 16-bit path): 16 codes in, two 16-byte chunks out
+      const uint8_t* wg = smem + warp * Ly::kWarp;
+      const uint8_t* k8 = wg + st * Ly::kStage;
+      const uint8_t* v8 = k8 + Ly::kTile8;
+      uint8_t* kw = const_cast<uint8_t*>(wg) + STAGES * Ly::kStage;
+      uint8_t* vw = kw + Ly::kTile;
+      constexpr int CPR8 = D / 16;
+#pragma unroll
+      for (int i = 0; i < kGrp * CPR8 / 32; ++i) {
+        const int idx = i * 32 + lane;
+        const int r = idx / CPR8, c = idx % CPR8;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint4 w = *reinterpret_cast<const uint4*>((t ? v8 : k8) + r * Ly::kRow8 + c * 16);
+          const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+          uint32_t h[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>(in[j >> 1] >> (16 * (j & 1))), __NV_E4M3);
+            h[j] = static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
+          }
+          uint8_t* dst = t ? vw : kw;
+          *reinterpret_cast<uint4*>(dst + swz(r, 2 * c, Ly::kRow)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(dst + swz(r, 2 * c + 1, Ly::kRow)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+      }
+      __syncwarp();
+      kb = wbase + STAGES * Ly::kStage;
+      vb = kb + Ly::kTile;
+    }
     const int p = p_lo + (warp + k * kWarps) * kGrp;
 
     // S (16 heads x 16 tokens) = Q K^T
@@ -168,8 +234,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
       const int ck = ks * 2 + ((lane >> 3) & 1);
       uint32_t b0, b1, b2, b3;
       ldsm_x4(kb + swz(tr, ck, Ly::kRow), b0, b1, b2, b3);
-      mma_bf16(sc[0], qa[ks], b0, b1);
-      mma_bf16(sc[1], qa[ks], b2, b3);
+      if (kFp8) {
+        mma_f16(sc[0], qa[ks], b0, b1);
+        mma_f16(sc[1], qa[ks], b2, b3);
+      } else {
+        mma_bf16(sc[0], qa[ks], b0, b1);
+        mma_bf16(sc[1], qa[ks], b2, b3);
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -206,8 +277,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
       o[i][2] *= al1;
       o[i][3] *= al1;
     }
-    const uint32_t pa[4] = {pack_bf16(sc[0][0], sc[0][1]), pack_bf16(sc[0][2], sc[0][3]),
-                            pack_bf16(sc[1][0], sc[1][1]), pack_bf16(sc[1][2], sc[1][3])};
+    uint32_t pa[4];
+    if (kFp8) {
+      pa[0] = pack_f16(sc[0][0], sc[0][1]);
+      pa[1] = pack_f16(sc[0][2], sc[0][3]);
+      pa[2] = pack_f16(sc[1][0], sc[1][1]);
+      pa[3] = pack_f16(sc[1][2], sc[1][3]);
+    } else {
+      pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+      pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+      pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+      pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+    }
     // O (16 heads x D) += P V
 #pragma unroll
     for (int dt2 = 0; dt2 < D / 16; ++dt2) {
@@ -215,8 +296,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
       const int ck = dt2 * 2 + (lane >> 4);
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(vb + swz(tr, ck, Ly::kRow), b0, b1, b2, b3);
-      mma_bf16(o[2 * dt2], pa, b0, b1);
-      mma_bf16(o[2 * dt2 + 1], pa, b2, b3);
+      if (kFp8) {
+        mma_f16(o[2 * dt2], pa, b0, b1);
+        mma_f16(o[2 * dt2 + 1], pa, b2, b3);
+      } else {
+        mma_bf16(o[2 * dt2], pa, b0, b1);
+        mma_bf16(o[2 * dt2 + 1], pa, b2, b3);
+      }
     }
     __syncwarp();
   }
@@ -263,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
       lsum += wt * mw[16 + rr];
       acc += wt * mw[32 + rr * D + d];
     }
+    if (kFp8) lsum *= a.inv_v_scale;  // out = acc * v_scale / l
     const int h = h0 + rr;
     if (nsplit == 1) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
@@ -316,15 +403,17 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
 }
 
 constexpr int kStages = 3;
+constexpr int kStages8 = 4;  // 8-bit stages are half the bytes: one more in flight
 
-template <int D>
+template <int D, bool kFp8>
 cudaError_t launch_decode_d(const AttnArgs& a, cudaStream_t st) {
-  using Ly = DecLayout<D, kStages>;
+  constexpr int kSt = kFp8 ? kStages8 : kStages;
+  using Ly = DecLayout<D, kSt, kFp8>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, kStages>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, kSt, kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -332,7 +421,7 @@ cudaError_t launch_decode_d(const AttnArgs& a, cudaStream_t st) {
   const int nhc = (a.group + 15) / 16;
   dim3 grid(a.nsplit, a.hkv * nhc, a.num_decode);
   count_launch();
-  decode_kernel<D, kStages><<<grid, kThreads, Ly::kBytes, st>>>(a);
+  decode_kernel<D, kSt, kFp8><<<grid, kThreads, Ly::kBytes, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.nsplit <= 1) return e;
   count_launch();
@@ -362,7 +451,9 @@ void decode_partition(int num_decode, int hkv_units, int max_seq_len, int num_sm
 
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t st) {
   if (a.num_decode <= 0) return cudaSuccess;
-  return a.head_dim == 128 ? launch_decode_d<128>(a, st) : launch_decode_d<64>(a, st);
+  if (a.kv_fp8)
+    return a.head_dim == 128 ? launch_decode_d<128, true>(a, st) : launch_decode_d<64, true>(a, st);
+  return a.head_dim == 128 ? launch_decode_d<128, false>(a, st) : launch_decode_d<64, false>(a, st);
 }
 
 }  // namespace pa

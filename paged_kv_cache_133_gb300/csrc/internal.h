@@ -51,6 +51,10 @@ struct AttnArgs {
   const void* v_new;
   int64_t kn_stride, vn_stride;
   const int32_t* slots;
+  // 8-bit cache: k_cache / v_cache hold E4M3 codes; scale_log2 then includes
+  // the K scale and the outputs are multiplied by the V scale (1 / inv_v_scale)
+  bool kv_fp8;
+  float inv_v_scale;
 };
 
 // Bytes at the start of the workspace reserved for the prefill work queue.
@@ -64,6 +68,10 @@ void decode_partition(int num_decode, int hkv_units, int max_seq_len, int num_sm
 cudaError_t launch_write_kv(const void* k, const void* v, int64_t ks, int64_t vs, void* kc,
                             void* vc, const int32_t* slots, int T, int num_blocks, int bs,
                             int row_elems, uint32_t* err, cudaStream_t st);
+cudaError_t launch_write_kv_fp8(const void* k, const void* v, int64_t ks, int64_t vs, void* kc,
+                                void* vc, const int32_t* slots, int T, int num_blocks, int bs,
+                                int row_elems, float inv_k_scale, float inv_v_scale,
+                                uint32_t* err, cudaStream_t st);
 cudaError_t launch_copy_blocks(void* kc, void* vc, const int32_t* pairs, int n, int num_blocks,
                                int block_elems, uint32_t* err, cudaStream_t st);
 cudaError_t launch_swap_blocks(const void* sk, const void* sv, void* dk, void* dv,

@@ -38,6 +38,48 @@ __global__ void __launch_bounds__(256) write_kv_kernel(const uint4* __restrict__
   }
 }
 
+// The scatter of an 8-bit cache: one thread per 8 elements (16 bytes in, 8
+// bytes out) of a token row.  Each element is multiplied by the reciprocal
+// scale in fp32 and rounded to the nearest E4M3 code, ties to even,
+// saturating at the largest finite magnitude.
+__global__ void __launch_bounds__(256) write_kv_fp8_kernel(const uint4* __restrict__ k,
+                                                           const uint4* __restrict__ v, int64_t ks,
+                                                           int64_t vs, uint2* __restrict__ kc,
+                                                           uint2* __restrict__ vc,
+                                                           const int32_t* __restrict__ slots,
+                                                           int T, int vec_per_row,
+                                                           int64_t num_slots, float inv_k,
+                                                           float inv_v, uint32_t* err) {
+  const int64_t total = static_cast<int64_t>(T) * vec_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / vec_per_row);
+    const int c = static_cast<int>(i - static_cast<int64_t>(t) * vec_per_row);
+    const int slot = __ldg(slots + t);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (c == 0) flag_error(err, PA_DEV_BAD_SLOT);
+      continue;
+    }
+    const int64_t o = static_cast<int64_t>(slot) * vec_per_row + c;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint4 w = __ldg(kv ? v + t * vs + c : k + t * ks + c);
+      const float inv = kv ? inv_v : inv_k;
+      const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+      uint32_t q[2] = {0u, 0u};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&in[p]);
+        const float2 f = make_float2(__low2float(b) * inv, __high2float(b) * inv);
+        const uint32_t two = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+        q[p >> 1] |= two << (16 * (p & 1));
+      }
+      (kv ? vc : kc)[o] = make_uint2(q[0], q[1]);
+    }
+  }
+}
+
 // blockIdx.y = pair; threads stride over the block's 16-byte pieces.
 // "vLLM 原理" §2.1: the fresh block receives the shared block's whole contents.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ kc,
@@ -101,6 +143,23 @@ cudaError_t launch_write_kv(const void* k, const void* v, int64_t ks, int64_t vs
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), ks / 8, vs / 8,
       static_cast<uint4*>(kc), static_cast<uint4*>(vc), slots, T, vpr,
       static_cast<int64_t>(num_blocks) * bs, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_write_kv_fp8(const void* k, const void* v, int64_t ks, int64_t vs, void* kc,
+                                void* vc, const int32_t* slots, int T, int num_blocks, int bs,
+                                int row_elems, float inv_k_scale, float inv_v_scale,
+                                uint32_t* err, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int vpr = row_elems / 8;
+  const int64_t total = static_cast<int64_t>(T) * vpr;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  count_launch();
+  write_kv_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), ks / 8, vs / 8,
+      static_cast<uint2*>(kc), static_cast<uint2*>(vc), slots, T, vpr,
+      static_cast<int64_t>(num_blocks) * bs, inv_k_scale, inv_v_scale, err);
   return cudaGetLastError();
 }
 
