@@ -441,6 +441,73 @@ def secondary(dev, steps, warmup, peaks):
     return res
 
 
+class Fp8Step:
+    """The decode workload with an 8-bit (E4M3) pool: pa_write_kv_fp8 + pa_attention_fp8."""
+
+    K_SCALE, V_SCALE = 0.03, 0.05
+
+    def __init__(self, lay, dev, seed=0):
+        import torch
+        import paged_kv_cache_133_gb300 as pa
+        self.pa, self.torch, self.lay = pa, torch, lay
+        g = workloads.make_tensors(lay, seed=seed, device=dev)
+        n_slots = lay.num_blocks * lay.block_size
+        rows = lambda c: c.view(n_slots, lay.num_kv_heads, lay.head_dim)
+        self.kc = torch.empty(g["k_cache"].shape, dtype=torch.uint8, device=dev)
+        self.vc = torch.empty_like(self.kc)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        all_slots = torch.arange(n_slots, dtype=torch.int32, device=dev)
+        pa.write_kv_fp8(rows(g["k_cache"]), rows(g["v_cache"]), self.kc, self.vc, all_slots,
+                        self.K_SCALE, self.V_SCALE, err=self.err)
+        self.q, self.k, self.v = g["q"], g["k"], g["v"]
+        del g
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        self.md = {
+            "qsl": torch.from_numpy(lay.query_start_loc).to(dev),
+            "seq_lens": torch.from_numpy(lay.seq_lens).to(dev),
+            "bt": torch.from_numpy(lay.block_tables).to(dev),
+            "slots": torch.from_numpy(lay.slot_mapping).to(dev),
+        }
+        self.out = torch.empty_like(self.q)
+        need = pa.workspace_size(lay.num_seqs, lay.num_q_heads, lay.num_kv_heads, lay.head_dim,
+                                 lay.max_seq_len)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+
+    def run(self, attn_events=None):
+        pa, md = self.pa, self.md
+        pa.write_kv_fp8(self.k, self.v, self.kc, self.vc, md["slots"], self.K_SCALE, self.V_SCALE,
+                        err=self.err)
+        if attn_events is not None:
+            attn_events[0].record()
+        pa.attention_fp8(self.q, self.kc, self.vc, md["qsl"], md["seq_lens"], md["bt"],
+                         k_scale=self.K_SCALE, v_scale=self.V_SCALE,
+                         max_seq_len=self.lay.max_seq_len, scale=self.lay.scale, out=self.out,
+                         workspace=self.ws, err=self.err)
+        if attn_events is not None:
+            attn_events[1].record()
+
+
+def fp8_leg(dev, steps, warmup, peaks, bf16_ms):
+    """Decode over an 8-bit pool: KV-read GB/s of the codes and tokens/s against bf16."""
+    lay = workloads.config_layout(2, 0)
+    st = Fp8Step(lay, dev)
+    ms, attn_ms, _ = time_device(st, steps, warmup, False)
+    kvb = kv_bytes(lay.seq_lens, lay.num_kv_heads, lay.head_dim, itemsize=1)
+    algo = kvb + 2 * lay.num_seqs * lay.num_q_heads * lay.head_dim * 2 + \
+        int(np.sum(-(-lay.seq_lens.astype(np.int64) // lay.block_size))) * 4
+    ach = algo / (attn_ms * 1e-3) / 1e9
+    res = {"workload": "decode batch (256 seqs, history U[512,4096], 32q/32kv, D 128, bs 16) on an E4M3 pool",
+           "metric": "decode KV-read GB/s (8-bit cache)", "value": kvb / (ms * 1e-3) / 1e9,
+           "ms_per_step": ms, "ms_attention": attn_ms, "kv_bytes_per_step": kvb,
+           "tokens_per_s": lay.num_tokens / (ms * 1e-3),
+           "speedup_vs_bf16_step": bf16_ms / ms,
+           "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
+                        "frac": ach / peaks["hbm"]}}
+    del st
+    return res
+
+
 def swap_leg(dev, iters=20, warmup=3, pairs=4096, seed=0):
     """Block swap between the device pool and a pool in page-locked host memory.
 
@@ -618,6 +685,8 @@ def main():
         del step
         torch.cuda.empty_cache()
         sec = secondary(dev, args.steps, args.warmup, peaks)
+        torch.cuda.empty_cache()
+        sec["decode_fp8"] = fp8_leg(dev, args.steps, args.warmup, peaks, ms)
     if rank != 0:
         if dist_on:
             import torch.distributed as dist

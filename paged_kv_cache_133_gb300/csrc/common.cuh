@@ -57,6 +57,22 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Four E4M3 codes (bytes 0..3 of w) as fp16: bytes 0, 1 -> lo, bytes 2, 3 -> hi.
+__device__ __forceinline__ void cvt_e4m3x4_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// 16 x 16 bytes transposed: lane L gets rows 4(L%4) .. +3 of column L/4 (r0)
+// and of column L/4 + 8 (r1); each lane passes the address of row L % 16.
+__device__ __forceinline__ void ldsm8_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0, %1}, [%2];\n"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
 // D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                         uint32_t b1) {

@@ -33,18 +33,24 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kGrp = 16;  // tokens per warp step
 
 // kFp8: the cache holds E4M3 codes.  The ring then stages the 8-bit rows
-// (plain layout), and each group is widened to fp16 (exact for every E4M3
-// value) into one swizzled K/V tile pair per warp before the products, which
-// then run as fp16 mma.sync with the query converted to fp16 once.
+// (row pitch D + 16 bytes against bank conflicts) and the products run as
+// fp16 mma.sync (every E4M3 value is exact in fp16), with the operand
+// fragments converted in registers straight from the staged codes:
+//  * K: the head dimension is read in a permuted order (the same for q and
+//    k, which leaves q.k unchanged) in which each lane's four dims of a
+//    16-dim step are four consecutive bytes: dims t * D/4 + 4 * step + j for
+//    lane t = lane % 4, so one 32-bit word per step and key;
+//  * V: the 8-bit transposing ldmatrix gives each lane four consecutive keys
+//    of one dimension; the keys of a group are permuted the same way in P
+//    (score column c of n-tile nt is key 4 (c / 2) + 2 nt + c % 2).
 template <int D, int STAGES, bool kFp8>
 struct DecLayout {
   static constexpr int kRow = D * 2;         // bytes of one token's K (or V) for one head
   static constexpr int kTile = kGrp * kRow;  // K or V of one group (16-bit)
-  static constexpr int kRow8 = D;            // 8-bit row
+  static constexpr int kRow8 = D + 16;       // staged 8-bit row (padded)
   static constexpr int kTile8 = kGrp * kRow8;
   static constexpr int kStage = kFp8 ? 2 * kTile8 : 2 * kTile;
-  static constexpr int kConv = kFp8 ? 2 * kTile : 0;  // widened K/V of the current group
-  static constexpr int kWarp = STAGES * kStage + kConv;
+  static constexpr int kWarp = STAGES * kStage;
   static constexpr int kLoop = kWarps * kWarp;
   static constexpr int kMergeFloats = 32 + 16 * D;  // m[16], l[16], acc[16][D]
   static constexpr int kMerge = kWarps * kMergeFloats * 4;
@@ -100,14 +106,25 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
       qa[ks][2] = va ? __ldg(pa_ + ks * 8 + 4) : 0u;
       qa[ks][3] = vb ? __ldg(pb_ + ks * 8 + 4) : 0u;
     }
-    if (kFp8) {  // bf16 -> fp16 pairs (exact in range for attention inputs)
+    if (kFp8) {
+      // permuted dims (see DecLayout): A regs {0,1} = dims t*D/4 + 4ks + {0,1},
+      // regs {2,3} = + {2,3}; bf16 -> fp16 pairs (exact in range)
+      const uint32_t* qa32 = reinterpret_cast<const uint32_t*>(
+          qrow + static_cast<int64_t>(h0 + (va ? r : 0)) * D + (lane & 3) * (D / 4));
+      const uint32_t* qb32 = reinterpret_cast<const uint32_t*>(
+          qrow + static_cast<int64_t>(h0 + (vb ? r + 8 : 0)) * D + (lane & 3) * (D / 4));
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
+      for (int ks = 0; ks < D / 16; ++ks) {
+        qa[ks][0] = va ? __ldg(qa32 + 2 * ks) : 0u;
+        qa[ks][1] = vb ? __ldg(qb32 + 2 * ks) : 0u;
+        qa[ks][2] = va ? __ldg(qa32 + 2 * ks + 1) : 0u;
+        qa[ks][3] = vb ? __ldg(qb32 + 2 * ks + 1) : 0u;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&qa[ks][j]);
           qa[ks][j] = pack_f16(__low2float(b), __high2float(b));
         }
+      }
     }
   }
 
@@ -189,55 +206,42 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
     cp_async_wait<STAGES - 1>();
     __syncwarp();
     const int st = k % STAGES;
-    uint32_t kb = wbase + st * Ly::kStage;
-    uint32_t vb = kb + Ly::kTile;
-    if (kFp8) {
-      // widen the staged 8-bit rows into this warp's fp16 tiles (same
-      // swizzle as the 16-bit path): 16 codes in, two 16-byte chunks out
-      const uint8_t* wg = smem + warp * Ly::kWarp;
-      const uint8_t* k8 = wg + st * Ly::kStage;
-      const uint8_t* v8 = k8 + Ly::kTile8;
-      uint8_t* kw = const_cast<uint8_t*>(wg) + STAGES * Ly::kStage;
-      uint8_t* vw = kw + Ly::kTile;
-      constexpr int CPR8 = D / 16;
-#pragma unroll
-      for (int i = 0; i < kGrp * CPR8 / 32; ++i) {
-        const int idx = i * 32 + lane;
-        const int r = idx / CPR8, c = idx % CPR8;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const uint4 w = *reinterpret_cast<const uint4*>((t ? v8 : k8) + r * Ly::kRow8 + c * 16);
-          const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-          uint32_t h[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
-                static_cast<__nv_fp8x2_storage_t>(in[j >> 1] >> (16 * (j & 1))), __NV_E4M3);
-            h[j] = static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
-          }
-          uint8_t* dst = t ? vw : kw;
-          *reinterpret_cast<uint4*>(dst + swz(r, 2 * c, Ly::kRow)) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(dst + swz(r, 2 * c + 1, Ly::kRow)) = make_uint4(h[4], h[5], h[6], h[7]);
-        }
-      }
-      __syncwarp();
-      kb = wbase + STAGES * Ly::kStage;
-      vb = kb + Ly::kTile;
-    }
+    const uint32_t kb = wbase + st * Ly::kStage;
+    const uint32_t vb = kb + (kFp8 ? Ly::kTile8 : Ly::kTile);
     const int p = p_lo + (warp + k * kWarps) * kGrp;
 
     // S (16 heads x 16 tokens) = Q K^T
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (kFp8) {
+      const uint8_t* k8 = smem + (kb - smem_u32(smem));
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const int tr = ((lane >> 4) << 3) + (lane & 7);
-      const int ck = ks * 2 + ((lane >> 3) & 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(kb + swz(tr, ck, Ly::kRow), b0, b1, b2, b3);
-      if (kFp8) {
-        mma_f16(sc[0], qa[ks], b0, b1);
-        mma_f16(sc[1], qa[ks], b2, b3);
-      } else {
+      for (int nt = 0; nt < 2; ++nt) {
+        const int n = lane >> 2;
+        const int key = 4 * (n >> 1) + 2 * nt + (n & 1);
+        const uint4* row = reinterpret_cast<const uint4*>(k8 + key * Ly::kRow8 + (lane & 3) * (D / 4));
+        uint32_t w[D / 16];
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x) {
+          const uint4 v4 = row[x];
+          w[4 * x] = v4.x;
+          w[4 * x + 1] = v4.y;
+          w[4 * x + 2] = v4.z;
+          w[4 * x + 3] = v4.w;
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t b0, b1;
+          cvt_e4m3x4_f16(w[ks], b0, b1);
+          mma_f16(sc[nt], qa[ks], b0, b1);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int tr = ((lane >> 4) << 3) + (lane & 7);
+        const int ck = ks * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + swz(tr, ck, Ly::kRow), b0, b1, b2, b3);
         mma_bf16(sc[0], qa[ks], b0, b1);
         mma_bf16(sc[1], qa[ks], b2, b3);
       }
@@ -246,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int pos = p + nt * 8 + (lane & 3) * 2 + (j & 1);
+        const int pos = kFp8 ? p + 4 * (lane & 3) + 2 * nt + (j & 1)
+                             : p + nt * 8 + (lane & 3) * 2 + (j & 1);
         sc[nt][j] = pos < p_hi ? sc[nt][j] * a.scale_log2 : -INFINITY;
       }
     float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
@@ -292,14 +297,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
     // O (16 heads x D) += P V
 #pragma unroll
     for (int dt2 = 0; dt2 < D / 16; ++dt2) {
-      const int tr = (((lane >> 3) & 1) << 3) + (lane & 7);
-      const int ck = dt2 * 2 + (lane >> 4);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(vb + swz(tr, ck, Ly::kRow), b0, b1, b2, b3);
       if (kFp8) {
+        // lane: keys 4t .. 4t+3 of dims dt2*16 + lane/4 (r0) and + 8 (r1)
+        uint32_t r0, r1, b0, b1, b2, b3;
+        ldsm8_t(vb + (lane & 15) * Ly::kRow8 + dt2 * 16, r0, r1);
+        cvt_e4m3x4_f16(r0, b0, b1);
+        cvt_e4m3x4_f16(r1, b2, b3);
         mma_f16(o[2 * dt2], pa, b0, b1);
         mma_f16(o[2 * dt2 + 1], pa, b2, b3);
       } else {
+        const int tr = (((lane >> 3) & 1) << 3) + (lane & 7);
+        const int ck = dt2 * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + swz(tr, ck, Ly::kRow), b0, b1, b2, b3);
         mma_bf16(o[2 * dt2], pa, b0, b1);
         mma_bf16(o[2 * dt2 + 1], pa, b2, b3);
       }
