@@ -38,6 +38,7 @@ int device_num_sms() {
 // steps sometimes let the decode grid fill every SM first and starve the
 // prefill (measured 1.22 against 0.92 ms on the mixed workload).
 struct SideStream {
+  int least = 0, greatest = 0;  // stream priority range of the device
   cudaStream_t hi = nullptr, lo = nullptr;
   cudaEvent_t fork = nullptr, join_hi = nullptr, join_lo = nullptr;
   bool ready = false;
@@ -59,6 +60,8 @@ static SideStream* side_stream() {
         cudaEventCreateWithFlags(&s.join_hi, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&s.join_lo, cudaEventDisableTiming) != cudaSuccess)
       return nullptr;
+    s.least = least;
+    s.greatest = greatest;
     s.ready = true;
   }
   return &s;
@@ -343,13 +346,23 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
     std::lock_guard<std::mutex> lock(g_side_mu);
     SideStream* side = side_stream();
     if (side) {
+      // The work counter is zeroed before the fork, so that in a captured
+      // graph both kernels become ready together and the priorities decide
+      // (a memset on the prefill side alone let the decode grid start first
+      // and fill the SMs).
+      if (cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st) != cudaSuccess)
+        return cuda_status(cudaGetLastError());
+      a.sched_zeroed = true;
       if (cudaEventRecord(side->fork, st) != cudaSuccess ||
           cudaStreamWaitEvent(side->hi, side->fork, 0) != cudaSuccess ||
           cudaStreamWaitEvent(side->lo, side->fork, 0) != cudaSuccess)
         return cuda_status(cudaGetLastError());
       a.max_ctas = device_num_sms() - reserve;
+      a.has_priority = true;
+      a.priority = side->greatest;
       int rc = cuda_status(launch_prefill(a, side->hi));
       if (rc != PA_OK) return rc;
+      a.priority = side->least;
       rc = cuda_status(launch_decode(a, side->lo));
       if (rc != PA_OK) return rc;
       if (cudaEventRecord(side->join_hi, side->hi) != cudaSuccess ||

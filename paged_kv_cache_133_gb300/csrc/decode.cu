@@ -431,12 +431,14 @@ cudaError_t launch_decode_d(const AttnArgs& a, cudaStream_t st) {
   const int nhc = (a.group + 15) / 16;
   dim3 grid(a.nsplit, a.hkv * nhc, a.num_decode);
   count_launch();
-  decode_kernel<D, kSt, kFp8><<<grid, kThreads, Ly::kBytes, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_prio(decode_kernel<D, kSt, kFp8>, grid, dim3(kThreads), Ly::kBytes, st,
+                              a.has_priority, a.priority, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || a.nsplit <= 1) return e;
   count_launch();
-  combine_kernel<D><<<dim3(a.num_decode, (a.hq + 3) / 4), 128, 0, st>>>(a);
-  return cudaGetLastError();
+  e = launch_prio(combine_kernel<D>, dim3(a.num_decode, (a.hq + 3) / 4), dim3(128), 0, st,
+                  a.has_priority, a.priority, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -40,7 +40,9 @@ struct AttnArgs {
   float* ws_o;   // [nsplit, num_decode, hq, head_dim]
   float* ws_ml;  // [nsplit, num_decode, hq, 2]
   // prefill work queue: a counter in the workspace header, zeroed per call
+  // (by the prefill launch, or before it when sched_zeroed)
   unsigned int* sched;
+  bool sched_zeroed;
   // cap on the persistent prefill grid (0: one CTA per SM)
   int max_ctas;
   // Fused scatter for the prefill rows (null k_new: none).  The tensor-core
@@ -55,7 +57,30 @@ struct AttnArgs {
   // the K scale and the outputs are multiplied by the V scale (1 / inv_v_scale)
   bool kv_fp8;
   float inv_v_scale;
+  // Launch priority of this call's attention kernels (has_priority false: the
+  // stream's own).  A mixed step sets it on both sides: the launch attribute
+  // is recorded in the kernel node when the step is captured into a CUDA graph.
+  bool has_priority;
+  int priority;
 };
+
+// Launches `kernel` on `st` with the given priority as a launch attribute when
+// `has_priority`, else with the stream's.
+template <typename... P, typename... A>
+cudaError_t launch_prio(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                        cudaStream_t st, bool has_priority, int priority, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributePriority;
+  attr[0].val.priority = priority;
+  cfg.attrs = attr;
+  cfg.numAttrs = has_priority ? 1u : 0u;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
 
 // Bytes at the start of the workspace reserved for the prefill work queue.
 constexpr size_t kWorkspaceHeader = 256;

@@ -829,12 +829,13 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   if (a.max_ctas > 0 && a.max_ctas < sms) sms = a.max_ctas;  // SMs left to a concurrent decode
   const int grid = total < sms ? total : sms;
   if (grid <= 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
+  cudaError_t e = a.sched_zeroed ? cudaSuccess : cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
   if (e != cudaSuccess) return e;
   count_launch();
-  prefill_tc_kernel<D, kFused><<<grid, kThreads, Ly::kAlloc, st>>>(mq, mk, mv, mo, mkn, mvn, a, total,
-                                                            max_level_of(a));
-  return cudaGetLastError();
+  const int max_level = max_level_of(a);
+  e = launch_prio(prefill_tc_kernel<D, kFused>, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
+                  a.has_priority, a.priority, mq, mk, mv, mo, mkn, mvn, a, total, max_level);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

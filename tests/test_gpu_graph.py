@@ -1,0 +1,81 @@
+"""Steps captured into a CUDA graph give the same results as the same calls
+run eagerly.  Every call is stream-ordered with no host sync, so a serving
+loop can capture one step and replay it; a mixed step forks its decode and
+prefill sides onto the library's two side streams and joins them back, which
+the capture records.  The kernels are deterministic, so the replayed output
+is compared bitwise with the eager one (and the eager one is checked against
+the oracle in the parity tests)."""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_133_gb300 as pa
+import workloads
+from tests import _helpers as H
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    H.ensure_built()
+    torch.cuda.set_device(0)
+
+
+def _layouts():
+    return [
+        # decode rows and two prefill chunks: the side-by-side dispatch
+        workloads.custom_layout("mixed", [300, 900, 40, 1200, 64, 0], [1, 1, 1, 1, 700, 333],
+                                16, 4, 128, 16, 400, 3),
+        # prefill only (persistent tensor-core kernel and its work counter)
+        workloads.custom_layout("prefill", [0, 0, 0], [500, 130, 47], 8, 2, 128, 16, 64, 4),
+        # decode only (split-KV partials and their combine)
+        workloads.custom_layout("decode", [5000, 17, 800], [1, 1, 1], 8, 8, 64, 16, 400, 5),
+    ]
+
+
+@pytest.mark.parametrize("lay", _layouts(), ids=lambda l: l.name)
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_graph_replay_matches_eager(lay, fused):
+    g = workloads.make_tensors(lay, seed=11, device=DEV)
+    md = H.device_meta(lay, DEV)
+    need = pa.workspace_size(lay.num_decode_seqs, lay.num_q_heads, lay.num_kv_heads,
+                             lay.head_dim, lay.max_seq_len)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kc0, vc0 = g["k_cache"].clone(), g["v_cache"].clone()
+
+    def step(out):
+        if fused:
+            pa.write_kv_attention(g["q"], g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"],
+                                  md["qsl"], md["seq_lens"], md["bt"],
+                                  num_decode_seqs=lay.num_decode_seqs,
+                                  max_query_len=lay.max_query_len, max_seq_len=lay.max_seq_len,
+                                  scale=lay.scale, out=out, workspace=ws, err=err)
+        else:
+            H.run_step(lay, g, md, err=err, out=out, workspace=ws)
+
+    eager = torch.empty_like(g["q"])
+    step(eager)
+    torch.cuda.synchronize()
+    kc1, vc1 = g["k_cache"].clone(), g["v_cache"].clone()
+
+    replay = torch.full_like(g["q"], float("nan"))
+    g["k_cache"].copy_(kc0)
+    g["v_cache"].copy_(vc0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(replay)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(replay.view(torch.int16), eager.view(torch.int16))
+    assert torch.equal(g["k_cache"].view(torch.int16), kc1.view(torch.int16))
+    assert torch.equal(g["v_cache"].view(torch.int16), vc1.view(torch.int16))
+    assert np.isfinite(H.f64(replay)).all()
