@@ -249,6 +249,34 @@ def time_device(step, steps, warmup, dist_on, clocks=None):
     return total / steps, attn, launches
 
 
+def time_graph(step, calls=10, replays=5):
+    """Device time per step (ms) with `calls` steps captured in one CUDA graph
+    and replayed (no host launch gaps); best of `replays` replays."""
+    torch = step.torch
+    for _ in range(3):
+        step.run()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(calls):
+            step.run()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(replays):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b) / calls)
+    del graph
+    return best
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -386,6 +414,7 @@ def secondary(dev, steps, warmup, peaks):
     lay = workloads.config_layout(3, 0)
     st = Step(lay, dev)
     ms, attn_ms, _ = time_device(st, steps, warmup, False)
+    msg = time_graph(st)
     fl = attention_flops(lay, np.arange(lay.num_seqs))
     tf = fl / (attn_ms * 1e-3) / 1e12
     del st
@@ -394,7 +423,7 @@ def secondary(dev, steps, warmup, peaks):
     res["prefill"] = {"workload": "16 prompts (log-uniform 16..2048, sum 8192), 32q/8kv, D 128, bs 16",
                       "fused_ms_per_step": msf, "fused_TFLOP/s_per_step": fl / (msf * 1e-3) / 1e12,
                       "metric": "prefill TFLOP/s", "value": tf, "ms_attention": attn_ms,
-                      "ms_per_step": ms, "flops": fl,
+                      "ms_per_step": ms, "graph_ms_per_step": msg, "flops": fl,
                       "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16"],
                                    "unit": "TFLOP/s", "frac": tf / peaks["bf16"]}}
     del st
@@ -420,6 +449,7 @@ def secondary(dev, steps, warmup, peaks):
     pre = np.arange(lay.num_decode_seqs, lay.num_seqs)
     t_star = decode_kernel_bytes(lay, dec) / (peaks["hbm"] * 1e9) + \
         attention_flops(lay, pre) / (peaks["bf16"] * 1e12)
+    ms4g = time_graph(st)
     del st
     st = Step(lay, dev, fused=True)
     ms4f, _, _ = time_device(st, steps, warmup, False)
@@ -435,6 +465,7 @@ def secondary(dev, steps, warmup, peaks):
     res["mixed"] = {"workload": "240 decodes (history U[128,8192]) + 2 chunks of 3976 on 1024/3000 cached, 32q/8kv",
                     "metric": "mixed-batch attn tokens/s", "value": lay.num_tokens / (ms * 1e-3),
                     "ms_per_step": ms, "ms_attention": attn_ms, "fused_ms_per_step": ms4f,
+                    "graph_ms_per_step": ms4g,
                     "additive_roofline_ms": t_star * 1e3, "frac": t_star * 1e3 / ms}
     del st
     res["swap"] = swap_leg(dev)
@@ -566,7 +597,10 @@ def swap_leg(dev, iters=20, warmup=3, pairs=4096, seed=0):
 
 
 def run_other(args, dev, peaks, rank, world, dist_on):
-    """One JSON line for the prefill, mixed or shared-prefix workload."""
+    """One JSON line for the prefill, mixed, shared-prefix or 8-bit decode workload."""
+    if args.workload == "decode_fp8":
+        run_fp8(args, dev, peaks, rank, world, dist_on)
+        return
     cfg = {"prefill": 3, "mixed": 4, "shared": 5, "prefix": 6}[args.workload]
     lay = workloads.config_layout(cfg, args.seed)
     step = Step(lay, dev, seed=args.seed + rank, fused=args.fused)
@@ -614,6 +648,37 @@ def run_other(args, dev, peaks, rank, world, dist_on):
     print(json.dumps(line), flush=True)
 
 
+def run_fp8(args, dev, peaks, rank, world, dist_on):
+    """One JSON line for the decode workload on an 8-bit (E4M3) pool."""
+    lay = workloads.config_layout(2, args.seed)
+    if args.decode_seqs:
+        lay = sample_layout(lay, np.arange(min(args.decode_seqs, lay.num_seqs)))
+        lay.num_blocks = int(lay.num_blocks * 1.1) + 1
+    step = Fp8Step(lay, dev, seed=args.seed + rank)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    ms, attn_ms, launches = time_device(step, args.steps, args.warmup, dist_on, clocks)
+    ms = _max_over_ranks(ms, dist_on, dev)
+    attn_ms = _max_over_ranks(attn_ms, dist_on, dev)
+    if int(step.err.item()):
+        raise RuntimeError(f"device error flag {int(step.err.item())}")
+    if rank != 0:
+        return
+    kvb = kv_bytes(lay.seq_lens, lay.num_kv_heads, lay.head_dim, itemsize=1)
+    algo = kvb + 2 * lay.num_seqs * lay.num_q_heads * lay.head_dim * 2 + \
+        int(np.sum(-(-lay.seq_lens.astype(np.int64) // lay.block_size))) * 4
+    ach = algo / (attn_ms * 1e-3) / 1e9
+    line = {"metric": "decode KV-read GB/s (8-bit cache)", "value": world * kvb / (ms * 1e-3) / 1e9,
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 cache, fp16 products", "data": "synthetic",
+            "config": {"workload": lay.name + " (E4M3 pool)", "ms_attention": attn_ms,
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm"]},
+            "cpu_baseline": None, "gpu_launches": launches, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -625,7 +690,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused", action="store_true",
                     help="time pa_write_kv_attention instead of pa_write_kv + pa_attention")
-    ap.add_argument("--workload", choices=["decode", "prefill", "mixed", "shared", "prefix"],
+    ap.add_argument("--workload",
+                    choices=["decode", "prefill", "mixed", "shared", "prefix", "decode_fp8"],
                     default="decode",
                     help="decode is the headline; the others print their own metric")
     ap.add_argument("--decode-seqs", type=int, default=0,
