@@ -210,6 +210,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
     const uint32_t vb = kb + (kFp8 ? Ly::kTile8 : Ly::kTile);
     const int p = p_lo + (warp + k * kWarps) * kGrp;
 
+    const bool full = p + kGrp <= p_hi;  // no key of the group is past the range
+
     // S (16 heads x 16 tokens) = Q K^T
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     if (kFp8) {
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
       for (int j = 0; j < 4; ++j) {
         const int pos = kFp8 ? p + 4 * (lane & 3) + 2 * nt + (j & 1)
                              : p + nt * 8 + (lane & 3) * 2 + (j & 1);
-        sc[nt][j] = pos < p_hi ? sc[nt][j] * a.scale_log2 : -INFINITY;
+        sc[nt][j] = full || pos < p_hi ? sc[nt][j] * a.scale_log2 : -INFINITY;
       }
     float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
     float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
@@ -260,7 +262,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    // The running max only moves when the group's max exceeds it by more than
+    // 8 (a factor 256): P then stays <= 256, and the numerator and the sum use
+    // the same reference, so the result does not depend on it.  O is rescaled
+    // only when some row's reference moved.
+    const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
+    const bool moved = __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1);
     const float r0 = mn0 == -INFINITY ? 0.f : mn0;
     const float r1 = mn1 == -INFINITY ? 0.f : mn1;
     const float al0 = ex2(m0 - r0), al1 = ex2(m1 - r1);
@@ -275,12 +282,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
     }
     l0 = l0 * al0 + (sc[0][0] + sc[0][1]) + (sc[1][0] + sc[1][1]);
     l1 = l1 * al1 + (sc[0][2] + sc[0][3]) + (sc[1][2] + sc[1][3]);
+    if (moved) {
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      o[i][0] *= al0;
-      o[i][1] *= al0;
-      o[i][2] *= al1;
-      o[i][3] *= al1;
+      for (int i = 0; i < D / 8; ++i) {
+        o[i][0] *= al0;
+        o[i][1] *= al0;
+        o[i][2] *= al1;
+        o[i][3] *= al1;
+      }
     }
     uint32_t pa[4];
     if (kFp8) {
