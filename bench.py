@@ -180,10 +180,11 @@ class Step:
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def run(self, attn_events=None, g=None, md=None):
+    def run(self, attn_events=None, g=None, md=None, out=None):
         pa, lay = self.pa, self.lay
         g = g or self.g
         md = md or self.md
+        out = self.out if out is None else out
         if len(lay.cow_pairs):
             pa.copy_blocks(g["k_cache"], g["v_cache"], md["pairs"], err=self.err)
         if self.fused:
@@ -193,7 +194,7 @@ class Step:
                                   md["qsl"], md["seq_lens"], md["bt"],
                                   num_decode_seqs=lay.num_decode_seqs,
                                   max_query_len=lay.max_query_len, max_seq_len=lay.max_seq_len,
-                                  scale=lay.scale, out=self.out, workspace=self.ws, err=self.err)
+                                  scale=lay.scale, out=out, workspace=self.ws, err=self.err)
             if attn_events is not None:
                 attn_events[1].record()
             return
@@ -202,7 +203,7 @@ class Step:
             attn_events[0].record()
         pa.attention(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"], md["bt"],
                      num_decode_seqs=lay.num_decode_seqs, max_query_len=lay.max_query_len,
-                     max_seq_len=lay.max_seq_len, scale=lay.scale, out=self.out,
+                     max_seq_len=lay.max_seq_len, scale=lay.scale, out=out,
                      workspace=self.ws, err=self.err)
         if attn_events is not None:
             attn_events[1].record()
@@ -285,42 +286,101 @@ class _Null:
         return False
 
 
+E2E_COPIES = ("pinned host -> device inputs and device -> pinned host output every step, "
+              "double-buffered on copy streams so that they overlap the neighbouring steps")
+
+
 def time_e2e(step, steps, warmup, dist_on):
     """Per-step time with the step's inputs copied in from pinned host memory
-    and the output read back, all inside the timed region."""
+    and the output read back, all inside the timed region.
+
+    The copies are pipelined as a serving loop would: inputs and outputs are
+    double-buffered on the device, the next step's inputs go up on a copy
+    stream while the current step computes, and the result comes back on a
+    second copy stream while the next step computes.  Returns (pipelined ms
+    per step, host-to-device bytes, device-to-host bytes, serial ms per step),
+    where the serial loop runs copy, step and read-back back to back."""
     torch = step.torch
-    lay = step.lay
     host = {k: step.g[k].cpu().pin_memory() for k in ("q", "k", "v")}
     for k in ("qsl", "seq_lens", "bt", "slots", "pairs"):
         host[k] = step.md[k].cpu().pin_memory()
-    dev_in = {k: torch.empty_like(step.g[k]) for k in ("q", "k", "v")}
-    dev_md = {k: torch.empty_like(step.md[k]) for k in step.md}
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    bufs = []
+    for _ in range(2):
+        bufs.append({"in": {k: torch.empty_like(step.g[k]) for k in ("q", "k", "v")},
+                     "md": {k: torch.empty_like(step.md[k]) for k in step.md},
+                     "out": torch.empty_like(step.out),
+                     "out_host": torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()})
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = bufs[0]["out_host"].numel() * bufs[0]["out_host"].element_size()
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
 
-    def one():
+    def upload(b):
         for k in ("q", "k", "v"):
-            dev_in[k].copy_(host[k], non_blocking=True)
-        for k in dev_md:
-            dev_md[k].copy_(host[k], non_blocking=True)
-        g = {"q": dev_in["q"], "k": dev_in["k"], "v": dev_in["v"],
+            b["in"][k].copy_(host[k], non_blocking=True)
+        for k in b["md"]:
+            b["md"][k].copy_(host[k], non_blocking=True)
+
+    def compute(b):
+        g = {"q": b["in"]["q"], "k": b["in"]["k"], "v": b["in"]["v"],
              "k_cache": step.g["k_cache"], "v_cache": step.g["v_cache"]}
-        step.run(g=g, md=dev_md)
-        out_host.copy_(step.out, non_blocking=True)
+        step.run(g=g, md=b["md"], out=b["out"])
+
+    def serial_step():
+        b = bufs[0]
+        upload(b)
+        compute(b)
+        b["out_host"].copy_(b["out"], non_blocking=True)
+
+    def pipelined(n):
+        """n steps; returns after queueing everything (the caller syncs)."""
+        in_ready, in_free, out_ready, out_free = ([ev(), ev()] for _ in range(4))
+        for i in range(2):  # buffers start free
+            in_free[i].record(comp)
+            out_free[i].record(comp)
+        with torch.cuda.stream(up):
+            up.wait_stream(comp)
+            upload(bufs[0])
+            in_ready[0].record(up)
+        for i in range(n):
+            b, nb = i % 2, (i + 1) % 2
+            if i + 1 < n:  # next step's inputs, once its buffer's last reader is done
+                with torch.cuda.stream(up):
+                    up.wait_event(in_free[nb])
+                    upload(bufs[nb])
+                    in_ready[nb].record(up)
+            comp.wait_event(in_ready[b])
+            comp.wait_event(out_free[b])
+            compute(bufs[b])
+            in_free[b].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_stream(comp)
+                bufs[b]["out_host"].copy_(bufs[b]["out"], non_blocking=True)
+                out_free[b].record(down)
+        comp.wait_stream(down)
+        comp.wait_stream(up)
 
     for _ in range(warmup):
-        one()
+        serial_step()
+    pipelined(max(warmup, 2))
     _barrier(dist_on)
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record()
     for _ in range(steps):
-        one()
+        serial_step()
+    e.record()
+    torch.cuda.synchronize()
+    serial_ms = s.elapsed_time(e) / steps
+    _barrier(dist_on)
+    torch.cuda.synchronize()
+    s.record()
+    pipelined(steps)
     e.record()
     torch.cuda.synchronize()
     _barrier(dist_on)
-    return s.elapsed_time(e) / steps, h2d, d2h
+    return s.elapsed_time(e) / steps, h2d, d2h, serial_ms
 
 
 # ---------------------------------------------------------------------------
@@ -608,7 +668,8 @@ def run_other(args, dev, peaks, rank, world, dist_on):
     ms, attn_ms, launches = time_device(step, args.steps, args.warmup, dist_on, clocks)
     ms = _max_over_ranks(ms, dist_on, dev)
     attn_ms = _max_over_ranks(attn_ms, dist_on, dev)
-    e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, dist_on)
+    e2e_ms, h2d, d2h, e2e_serial_ms = time_e2e(step, args.steps, args.warmup, dist_on)
+    e2e_serial_ms = _max_over_ranks(e2e_serial_ms, dist_on, dev)
     e2e_ms = _max_over_ranks(e2e_ms, dist_on, dev)
     if rank != 0:
         return
@@ -643,7 +704,8 @@ def run_other(args, dev, peaks, rank, world, dist_on):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roof, "cpu_baseline": None,
             "e2e": {"value": e2e_v, "unit": unit, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "copies": E2E_COPIES,
+                    "serial_ms_per_step": e2e_serial_ms},
             "gpu_launches": launches, "clocks": clocks.summary()}
     print(json.dumps(line), flush=True)
 
@@ -740,7 +802,8 @@ def main():
     achieved = algo / (attn_ms * 1e-3) / 1e9
     digest = source_digest("decode.cu")
     traffic = measured_traffic("decode_kernel", "decode", digest)
-    e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, dist_on)
+    e2e_ms, h2d, d2h, e2e_serial_ms = time_e2e(step, args.steps, args.warmup, dist_on)
+    e2e_serial_ms = _max_over_ranks(e2e_serial_ms, dist_on, dev)
     e2e_ms = _max_over_ranks(e2e_ms, dist_on, dev)
     step.fused = True  # the same step through pa_write_kv_attention, for reference
     fused_ms, _, _ = time_device(step, max(args.steps // 4, 1), args.warmup, dist_on)
@@ -776,7 +839,8 @@ def main():
                      "ms_per_launch": attn_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": world * kvb / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": E2E_COPIES, "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": launches,
         "clocks": clocks.summary(),
     }
