@@ -161,11 +161,12 @@ class ClockSampler:
 class Step:
     """Device-resident inputs of one workload and the calls of one step."""
 
-    def __init__(self, lay, dev, seed=0, fused=False):
+    def __init__(self, lay, dev, seed=0, fused=False, prefix_blocks=0):
         import torch
         import paged_kv_cache_133_gb300 as pa
         self.pa, self.torch, self.lay, self.dev = pa, torch, lay, dev
         self.fused = fused  # one pa_write_kv_attention call instead of pa_write_kv + pa_attention
+        self.prefix_blocks = prefix_blocks  # > 0: pa_attention_cascade over a shared prefix
         self.g = workloads.make_tensors(lay, seed=seed, device=dev)
         self.md = {
             "qsl": torch.from_numpy(lay.query_start_loc).to(dev),
@@ -177,6 +178,10 @@ class Step:
         self.out = torch.empty_like(self.g["q"])
         need = pa.workspace_size(lay.num_decode_seqs, lay.num_q_heads, lay.num_kv_heads,
                                  lay.head_dim, lay.max_seq_len)
+        if prefix_blocks:
+            need = pa.cascade_workspace_size(lay.num_seqs, lay.num_q_heads, lay.num_kv_heads,
+                                             lay.head_dim, lay.max_seq_len, prefix_blocks,
+                                             lay.block_size)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -201,6 +206,14 @@ class Step:
         pa.write_kv(g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"], err=self.err)
         if attn_events is not None:
             attn_events[0].record()
+        if self.prefix_blocks:
+            pa.attention_cascade(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"],
+                                 md["bt"], prefix_blocks=self.prefix_blocks,
+                                 max_seq_len=lay.max_seq_len, scale=lay.scale, out=out,
+                                 workspace=self.ws, err=self.err)
+            if attn_events is not None:
+                attn_events[1].record()
+            return
         pa.attention(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"], md["bt"],
                      num_decode_seqs=lay.num_decode_seqs, max_query_len=lay.max_query_len,
                      max_seq_len=lay.max_seq_len, scale=lay.scale, out=out,
@@ -468,6 +481,15 @@ def run_reference(args, rank):
 
 # ---------------------------------------------------------------------------
 
+def shared_prefix_blocks(lay):
+    """Leading block-table entries that every sequence shares."""
+    tabs = [list(t) for t in lay.tables]
+    n = 0
+    while all(len(t) > n for t in tabs) and len({t[n] for t in tabs}) == 1:
+        n += 1
+    return n
+
+
 def secondary(dev, steps, warmup, peaks):
     """Prefill and mixed-step measurements (device time only)."""
     res = {}
@@ -517,10 +539,18 @@ def secondary(dev, steps, warmup, peaks):
     lay5 = workloads.config_layout(5, 0)
     st = Step(lay5, dev)
     ms5, attn5, _ = time_device(st, steps, warmup, False)
+    del st
+    pb5 = shared_prefix_blocks(lay5)
+    st = Step(lay5, dev, prefix_blocks=pb5)
+    ms5c, attn5c, _ = time_device(st, steps, warmup, False)
     kvb5 = kv_bytes(lay5.seq_lens, lay5.num_kv_heads, lay5.head_dim)
     res["shared"] = {"workload": "64 seqs sharing a 16384-token prompt (63 copy-on-write pairs), tails U[1,256], 64q/8kv",
                      "metric": "logical KV-read GB/s", "value": kvb5 / (ms5 * 1e-3) / 1e9,
                      "ms_per_step": ms5, "ms_attention": attn5,
+                     "cascade": {"prefix_blocks": pb5, "ms_per_step": ms5c, "ms_attention": attn5c,
+                                 "value": kvb5 / (ms5c * 1e-3) / 1e9,
+                                 "call": "pa_attention_cascade: the shared prefix read once per 64 "
+                                         "query rows of a kv head, merged with each sequence's own keys"},
                      "note": "the shared prefix (67 MB of K+V) stays in L2; logical bytes count it once per sequence"}
     res["mixed"] = {"workload": "240 decodes (history U[128,8192]) + 2 chunks of 3976 on 1024/3000 cached, 32q/8kv",
                     "metric": "mixed-batch attn tokens/s", "value": lay.num_tokens / (ms * 1e-3),
@@ -663,7 +693,8 @@ def run_other(args, dev, peaks, rank, world, dist_on):
         return
     cfg = {"prefill": 3, "mixed": 4, "shared": 5, "prefix": 6}[args.workload]
     lay = workloads.config_layout(cfg, args.seed)
-    step = Step(lay, dev, seed=args.seed + rank, fused=args.fused)
+    pb = shared_prefix_blocks(lay) if args.cascade and args.workload == "shared" else 0
+    step = Step(lay, dev, seed=args.seed + rank, fused=args.fused, prefix_blocks=pb)
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     ms, attn_ms, launches = time_device(step, args.steps, args.warmup, dist_on, clocks)
     ms = _max_over_ranks(ms, dist_on, dev)
@@ -701,6 +732,7 @@ def run_other(args, dev, peaks, rank, world, dist_on):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": lay.name, "ms_attention": attn_ms, "fused": bool(args.fused),
+                       "cascade_prefix_blocks": pb,
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roof, "cpu_baseline": None,
             "e2e": {"value": e2e_v, "unit": unit, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
@@ -756,6 +788,8 @@ def main():
                     choices=["decode", "prefill", "mixed", "shared", "prefix", "decode_fp8"],
                     default="decode",
                     help="decode is the headline; the others print their own metric")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared workload: pa_attention_cascade over the common prefix blocks")
     ap.add_argument("--decode-seqs", type=int, default=0,
                     help="profile case: only the first N decode sequences, pool sized to fit")
     args = ap.parse_args()

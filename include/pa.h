@@ -274,6 +274,45 @@ int pa_attention_noalloc(void* out, int64_t out_stride_t, const void* q, int64_t
                          int block_size, int num_blocks, float scale, uint32_t* err_flag,
                          void* stream);
 
+/*
+ * pa_attention_cascade — decode attention for a batch whose sequences all
+ * start with the same cached blocks: a common prompt served from the prefix
+ * cache ("vLLM 原理" §2.3 Automatic Prefix Cache), whose shared blocks
+ * copy-on-write keeps read-only (§2.1).
+ *
+ * Same result, within rounding, as pa_attention with num_decode_seqs =
+ * num_seqs (every row a decode row) and max_query_len = 1.  The caller
+ * promises that the first prefix_blocks entries of every block_tables row
+ * hold the same physical block ids, so that key positions
+ * [0, prefix_blocks * block_size) are the same K/V for every sequence.  The
+ * host scheduler knows this from the tables it built.  The call then reads
+ * those keys once for each group of 64 (sequence, query head) rows of a kv
+ * head instead of once per sequence, reads each sequence's own keys
+ * [prefix_blocks * block_size, L) as pa_attention does, and merges the two
+ * exactly (online-softmax partials).
+ *
+ * Arguments: those of pa_attention without num_decode_seqs and
+ * max_query_len, plus prefix_blocks (>= 0; 0 is plain decode attention).
+ * bf16 cache only.  Workspace: pa_cascade_workspace_size(...) bytes.
+ * Errors: PA_ERR_INVALID_ARG when prefix_blocks < 0, prefix_blocks >
+ * max_blocks_per_seq or prefix_blocks * block_size >= max_seq_len.  Device
+ * errors are those of pa_attention.  A sequence with seq_len <=
+ * prefix_blocks * block_size has no key of its own and sets PA_DEV_BAD_LEN;
+ * its output row is not written.  Tables that break the promise give the
+ * attention of the first sequence's prefix blocks, which is undefined for
+ * the others (not detected).
+ */
+size_t pa_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_seq_len, int prefix_blocks, int block_size);
+int pa_attention_cascade(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                         const void* k_cache, const void* v_cache,
+                         const int32_t* query_start_loc, const int32_t* seq_lens,
+                         const int32_t* block_tables, int num_seqs, int num_tokens,
+                         int max_blocks_per_seq, int max_seq_len, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         int prefix_blocks, float scale, void* workspace, size_t workspace_bytes,
+                         uint32_t* err_flag, void* stream);
+
 /* Human-readable name of a pa_status value (static string). */
 const char* pa_status_string(int status);
 

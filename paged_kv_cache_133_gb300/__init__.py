@@ -7,6 +7,7 @@ library has not been built the first call raises.
 
     write_kv(k, v, k_cache, v_cache, slot_mapping)
     attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, ...)
+    attention_cascade(..., prefix_blocks=...)   # decode over a shared cached prefix
     copy_blocks(k_cache, v_cache, pairs)
 """
 
@@ -17,7 +18,8 @@ import math
 import os
 
 __all__ = ["write_kv", "attention", "write_kv_attention", "attention_noalloc", "copy_blocks",
-           "swap_blocks", "write_kv_fp8", "attention_fp8", "workspace_size", "kernel_launches",
+           "swap_blocks", "write_kv_fp8", "attention_fp8", "attention_cascade", "workspace_size",
+           "cascade_workspace_size", "kernel_launches",
            "library_path", "load", "PaError", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN",
            "DEV_BAD_DECODE", "DEV_BAD_PAIR"]
 
@@ -53,6 +55,10 @@ _SIGNATURES = {
     "pa_attention_fp8": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i,
                                 _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_f, _c_f,
                                 _c_f, _c_p, _c_sz, _c_p, _c_p]),
+    "pa_cascade_workspace_size": (_c_sz, [_c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i]),
+    "pa_attention_cascade": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i,
+                                    _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_f,
+                                    _c_p, _c_sz, _c_p, _c_p]),
     "pa_copy_blocks": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_p, _c_p]),
     "pa_attention_noalloc": (_c_i, [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i,
                                     _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
@@ -211,6 +217,51 @@ def attention_fp8(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, 
                                  max_seq_len, hq, hkv, d, bs, nb, float(scale), float(k_scale),
                                  float(v_scale), _ptr(workspace), wbytes, _ptr(err), _stream(stream))
     _check(rc, "pa_attention_fp8")
+    return out
+
+
+def cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                           prefix_blocks, block_size) -> int:
+    return int(load().pa_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 max_seq_len, prefix_blocks, block_size))
+
+
+def attention_cascade(q, k_cache, v_cache, query_start_loc, seq_lens, block_tables, *,
+                      prefix_blocks, max_seq_len, scale=None, out=None, workspace=None, err=None,
+                      stream=None):
+    """Decode attention when every sequence's first ``prefix_blocks`` table
+    entries are the same physical blocks (a shared cached prompt); every
+    sequence is a decode row."""
+    import torch
+    _bf16_rows(q, "q")
+    _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
+                 (block_tables, "block_tables")):
+        _i32(t, n)
+    _need(block_tables.dim() == 2, "block_tables must be [num_seqs, max_blocks_per_seq]")
+    nb, bs, hkv, d = k_cache.shape
+    T, hq, dq = q.shape
+    _need(dq == d, "q head_dim differs from the cache's")
+    S = seq_lens.numel()
+    _need(query_start_loc.numel() == S + 1 and block_tables.shape[0] == S, "metadata sizes differ")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _bf16_rows(out, "out")
+        _need(out.shape == q.shape, "out shape differs from q")
+    need = cascade_workspace_size(S, hq, hkv, d, max_seq_len, prefix_blocks, bs)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load().pa_attention_cascade(_ptr(out), out.stride(0), _ptr(q), q.stride(0), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(query_start_loc), _ptr(seq_lens),
+                                     _ptr(block_tables), S, T, block_tables.shape[1], max_seq_len,
+                                     hq, hkv, d, bs, nb, int(prefix_blocks), float(scale),
+                                     _ptr(workspace), wbytes, _ptr(err), _stream(stream))
+    _check(rc, "pa_attention_cascade")
     return out
 
 

@@ -108,6 +108,26 @@ static size_t decode_workspace(int num_decode, int hq, int hkv, int head_dim, in
   return static_cast<size_t>(*nsplit) * num_decode * hq * (head_dim + 2) * sizeof(float);
 }
 
+// Cascade: suffix splits over the longest own-key range and prefix chunks;
+// partials of both for every (decode sequence, query head).
+static size_t cascade_workspace(int num_decode, int hq, int hkv, int head_dim, int max_seq_len,
+                                int prefix_len, int* part, int* nsplit, int* part_p,
+                                int* nsplit_p) {
+  *part = 64;
+  *nsplit = 1;
+  *part_p = 64;
+  *nsplit_p = 0;
+  if (num_decode <= 0 || hkv <= 0 || hq <= 0 || hq % hkv || prefix_len <= 0 ||
+      max_seq_len <= prefix_len)
+    return 0;
+  const int group = hq / hkv;
+  const int units = hkv * ((group + 15) / 16);
+  decode_partition(num_decode, units, max_seq_len - prefix_len, device_num_sms(), part, nsplit);
+  cascade_partition(num_decode, hq, hkv, prefix_len, device_num_sms(), part_p, nsplit_p);
+  return static_cast<size_t>(*nsplit + *nsplit_p) * num_decode * hq * (head_dim + 2) *
+         sizeof(float);
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -239,7 +259,8 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
                           int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
                           int block_size, int num_blocks, float scale, void* workspace,
                           size_t workspace_bytes, uint32_t* err_flag, void* stream,
-                          const FusedIn* fused, const float* kv_scales = nullptr) {
+                          const FusedIn* fused, const float* kv_scales = nullptr,
+                          int prefix_blocks = 0) {
   if (num_seqs < 0 || num_tokens < 0 || num_decode_seqs < 0 || num_decode_seqs > num_seqs ||
       max_query_len < 0 || max_seq_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq <= 0)
@@ -291,17 +312,32 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
   a.err = err_flag;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t decode_need = num_decode_seqs > 0 && max_seq_len > 0
-                                 ? decode_workspace(num_decode_seqs, num_q_heads, num_kv_heads,
-                                                    head_dim, max_seq_len, &a.part, &a.nsplit)
-                                 : 0;
+  size_t decode_need = 0;
+  if (prefix_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (prefix_blocks > 0) {
+    // Shared-prefix decode: decode rows only, bf16 cache, no fused scatter.
+    if (num_decode_seqs != num_seqs || fused || kv_scales) return PA_ERR_UNSUPPORTED;
+    const int64_t plen = static_cast<int64_t>(prefix_blocks) * block_size;
+    if (prefix_blocks > max_blocks_per_seq || plen >= max_seq_len) return PA_ERR_INVALID_ARG;
+    a.cascade = true;
+    a.prefix_len = static_cast<int>(plen);
+    a.key_begin = a.prefix_len;
+    decode_need = cascade_workspace(num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
+                                    max_seq_len, a.prefix_len, &a.part, &a.nsplit,
+                                    &a.part_prefix, &a.nsplit_prefix);
+    a.split0 = a.nsplit_prefix;
+  } else if (num_decode_seqs > 0 && max_seq_len > 0) {
+    decode_need = decode_workspace(num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
+                                   max_seq_len, &a.part, &a.nsplit);
+  }
   if (!workspace || workspace_bytes < kWorkspaceHeader + decode_need ||
       (reinterpret_cast<uintptr_t>(workspace) & 15u))
     return PA_ERR_WORKSPACE;
   a.sched = static_cast<unsigned int*>(workspace);
   if (decode_need > 0) {
     a.ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader);
-    a.ws_ml = a.ws_o + static_cast<size_t>(a.nsplit) * num_decode_seqs * num_q_heads * head_dim;
+    a.ws_ml = a.ws_o + static_cast<size_t>(a.nsplit + a.nsplit_prefix) * num_decode_seqs *
+                           num_q_heads * head_dim;
   }
   const bool has_decode = num_decode_seqs > 0 && max_seq_len > 0;
   const bool has_prefill = num_seqs > num_decode_seqs && max_query_len > 0;
@@ -372,6 +408,10 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
         return cuda_status(cudaGetLastError());
       return PA_OK;
     }
+  }
+  if (a.cascade) {  // prefix partials, then the own keys and the combine
+    int rc = cuda_status(launch_cascade_prefix(a, st));
+    if (rc != PA_OK) return rc;
   }
   if (has_decode) {
     int rc = cuda_status(launch_decode(a, st));
@@ -460,6 +500,32 @@ int pa_attention_fp8(void* out, int64_t out_stride_t, const void* q, int64_t q_s
                         num_decode_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
                         head_dim, block_size, num_blocks, scale, workspace, workspace_bytes,
                         err_flag, stream, nullptr, scales);
+}
+
+
+size_t pa_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_seq_len, int prefix_blocks, int block_size) {
+  int part, nsplit, part_p, nsplit_p;
+  const int64_t plen = static_cast<int64_t>(prefix_blocks) * block_size;
+  if (prefix_blocks <= 0 || block_size <= 0 || plen >= max_seq_len)
+    return pa_attention_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len);
+  return kWorkspaceHeader + cascade_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              max_seq_len, static_cast<int>(plen), &part, &nsplit,
+                                              &part_p, &nsplit_p);
+}
+
+int pa_attention_cascade(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
+                         const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
+                         const int32_t* seq_lens, const int32_t* block_tables, int num_seqs,
+                         int num_tokens, int max_blocks_per_seq, int max_seq_len,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, int prefix_blocks, float scale, void* workspace,
+                         size_t workspace_bytes, uint32_t* err_flag, void* stream) {
+  return attention_impl(out, out_stride_t, q, q_stride_t, k_cache, v_cache, query_start_loc,
+                        seq_lens, block_tables, num_seqs, num_tokens, max_blocks_per_seq,
+                        num_seqs, 1, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                        num_blocks, scale, workspace, workspace_bytes, err_flag, stream, nullptr,
+                        nullptr, prefix_blocks);
 }
 
 }  // extern "C"

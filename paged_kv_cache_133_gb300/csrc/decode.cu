@@ -80,9 +80,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
     if (reporter) flag_error(a.err, PA_DEV_BAD_LEN);
     return;
   }
-  const int nsplit = (L + a.part - 1) / a.part;
+  // Keys [key_begin, L); key_begin > 0 only in the suffix pass of a cascade,
+  // which needs a key of the sequence's own past the shared prefix.
+  if (L <= a.key_begin) {
+    if (reporter) flag_error(a.err, PA_DEV_BAD_LEN);
+    return;
+  }
+  const int nsplit = (L - a.key_begin + a.part - 1) / a.part;
   if (split >= nsplit) return;
-  const int p_lo = split * a.part;
+  const int p_lo = a.key_begin + split * a.part;
   const int p_hi = min(L, p_lo + a.part);
   const int ngroups = (p_hi - p_lo + kGrp - 1) / kGrp;
   const int rows = min(16, a.group - hc * 16);  // live query heads in this CTA
@@ -370,12 +376,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnArgs a) {
     }
     if (kFp8) lsum *= a.inv_v_scale;  // out = acc * v_scale / l
     const int h = h0 + rr;
-    if (nsplit == 1) {
+    if (nsplit == 1 && !a.cascade) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
       out[static_cast<int64_t>(t0) * a.out_stride + static_cast<int64_t>(h) * D + d] =
           __float2bfloat16_rn(acc / lsum);
     } else {
-      const int64_t row = (static_cast<int64_t>(split) * a.num_decode + s) * a.hq + h;
+      const int64_t row = (static_cast<int64_t>(a.split0 + split) * a.num_decode + s) * a.hq + h;
       a.ws_o[row * D + d] = acc;
       if (d == 0) {
         a.ws_ml[row * 2] = M;
@@ -398,7 +404,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   if (qn != 1 || t0 < 0 || t0 >= a.num_tokens || L < 1 || L > a.max_seq_len ||
       L > (a.max_blocks << a.bs_log2))
     return;
-  const int n = (L + a.part - 1) / a.part;
+  if (L <= a.key_begin) return;
+  // prefix partials (cascade) first, then this row's splits of [key_begin, L)
+  const int n = a.nsplit_prefix + (L - a.key_begin + a.part - 1) / a.part;
   if (n <= 1) return;
   const int64_t stride = static_cast<int64_t>(a.num_decode) * a.hq;
   const int64_t row0 = static_cast<int64_t>(s) * a.hq + h;
@@ -443,7 +451,7 @@ cudaError_t launch_decode_d(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e = launch_prio(decode_kernel<D, kSt, kFp8>, grid, dim3(kThreads), Ly::kBytes, st,
                               a.has_priority, a.priority, a);
   if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess || a.nsplit <= 1) return e;
+  if (e != cudaSuccess || (a.nsplit <= 1 && !a.cascade)) return e;
   count_launch();
   e = launch_prio(combine_kernel<D>, dim3(a.num_decode, (a.hq + 3) / 4), dim3(128), 0, st,
                   a.has_priority, a.priority, a);

@@ -57,6 +57,13 @@ struct AttnArgs {
   // the K scale and the outputs are multiplied by the V scale (1 / inv_v_scale)
   bool kv_fp8;
   float inv_v_scale;
+  // Shared-prefix (cascade) decode: the first prefix_len key positions of every
+  // decode sequence are the same physical blocks.  The prefix pass writes
+  // nsplit_prefix partials per (sequence, head) into workspace slots
+  // [0, nsplit_prefix); the decode kernel then covers keys [key_begin, L) and
+  // writes its partials from slot split0 on; the combine merges them all.
+  bool cascade;
+  int key_begin, split0, nsplit_prefix, prefix_len, part_prefix;
   // Launch priority of this call's attention kernels (has_priority false: the
   // stream's own).  A mixed step sets it on both sides: the launch attribute
   // is recorded in the kernel node when the step is captured into a CUDA graph.
@@ -103,6 +110,11 @@ cudaError_t launch_swap_blocks(const void* sk, const void* sv, void* dk, void* d
                                const int32_t* pairs, int n, int src_blocks, int dst_blocks,
                                int block_elems, uint32_t* err, cudaStream_t st);
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t st);
+// Cascade prefix pass (see AttnArgs::cascade); CTAs and slots from
+// cascade_partition.
+cudaError_t launch_cascade_prefix(const AttnArgs& a, cudaStream_t st);
+void cascade_partition(int num_decode, int hq, int hkv, int prefix_len, int num_sms,
+                       int* part_prefix, int* nsplit_prefix);
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t st);
 
 // Tensor-core (tcgen05) prefill: whether the shapes and the environment allow
