@@ -549,7 +549,7 @@ def secondary(dev, steps, warmup, peaks):
                      "ms_per_step": ms5, "ms_attention": attn5,
                      "cascade": {"prefix_blocks": pb5, "ms_per_step": ms5c, "ms_attention": attn5c,
                                  "value": kvb5 / (ms5c * 1e-3) / 1e9,
-                                 "call": "pa_attention_cascade: the shared prefix read once per 64 "
+                                 "call": "pa_attention_cascade: the shared prefix read once per 128 "
                                          "query rows of a kv head, merged with each sequence's own keys"},
                      "note": "the shared prefix (67 MB of K+V) stays in L2; logical bytes count it once per sequence"}
     res["mixed"] = {"workload": "240 decodes (history U[128,8192]) + 2 chunks of 3976 on 1024/3000 cached, 32q/8kv",

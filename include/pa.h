@@ -286,7 +286,7 @@ int pa_attention_noalloc(void* out, int64_t out_stride_t, const void* q, int64_t
  * hold the same physical block ids, so that key positions
  * [0, prefix_blocks * block_size) are the same K/V for every sequence.  The
  * host scheduler knows this from the tables it built.  The call then reads
- * those keys once for each group of 64 (sequence, query head) rows of a kv
+ * those keys once for each group of 128 (sequence, query head) rows of a kv
  * head instead of once per sequence, reads each sequence's own keys
  * [prefix_blocks * block_size, L) as pa_attention does, and merges the two
  * exactly (online-softmax partials).

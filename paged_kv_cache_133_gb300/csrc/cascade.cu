@@ -5,17 +5,17 @@
 // read-only).  When every decode sequence of a step starts with the same P
 // key positions (the same physical blocks), the split-KV decode kernel would
 // read those P keys once per sequence.  This pass reads them once per group
-// of 64 query rows instead: for every (decode sequence, query head) row it
+// of 128 query rows instead: for every (decode sequence, query head) row it
 // computes the online-softmax partial (m, l, acc) over the prefix keys.  The
 // decode kernel then covers each sequence's own keys [P, L), and the combine
 // merges both with the split-KV merge (m = max_j m_j,
 // l = sum_j l_j 2^(m_j - m), o = sum_j acc_j 2^(m_j - m) / l), which is exact
 // for any partition of the keys.
 //
-// CTA: 64 query rows of one kv head (4 warps x 16 rows) and one chunk of the
-// prefix.  Row r of a kv head's rows is (decode sequence r / g, query head
+// CTA: 128 query rows of one kv head (8 warps x 16 rows) and one chunk of the
+// prefix; two CTAs per SM (128 registers a thread).  Row r of a kv head's rows is (decode sequence r / g, query head
 // hk * g + r % g), g = query heads per kv head.  The chunk's keys stream
-// through a 3-stage ring of 64-key stages (the kv head's K and V rows, 16-byte
+// through a 3-stage ring of 32-key stages (the kv head's K and V rows, 16-byte
 // cp.async by all threads, block ids from the first sequence's table); every
 // warp runs each stage against its own 16 rows: q.k and p.v as m16n8k16 bf16
 // mma.sync with fp32 accumulation, scores in the log2 domain, and a running
@@ -29,10 +29,10 @@ namespace pa {
 
 namespace {
 
-constexpr int kCWarps = 4;
+constexpr int kCWarps = 8;
 constexpr int kCThreads = kCWarps * 32;
 constexpr int kCRows = kCWarps * 16;  // query rows per CTA
-constexpr int kCKeys = 64;            // keys per stage
+constexpr int kCKeys = 32;            // keys per stage
 constexpr int kCStages = 3;
 
 template <int D>
