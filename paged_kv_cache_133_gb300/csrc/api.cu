@@ -111,7 +111,7 @@ static size_t decode_workspace(int num_decode, int hq, int hkv, int head_dim, in
 // Cascade: suffix splits over the longest own-key range and prefix chunks;
 // partials of both for every (decode sequence, query head).
 static size_t cascade_workspace(int num_decode, int hq, int hkv, int head_dim, int max_seq_len,
-                                int prefix_len, int* part, int* nsplit, int* part_p,
+                                int prefix_len, bool tc, int* part, int* nsplit, int* part_p,
                                 int* nsplit_p) {
   *part = 64;
   *nsplit = 1;
@@ -123,7 +123,7 @@ static size_t cascade_workspace(int num_decode, int hq, int hkv, int head_dim, i
   const int group = hq / hkv;
   const int units = hkv * ((group + 15) / 16);
   decode_partition(num_decode, units, max_seq_len - prefix_len, device_num_sms(), part, nsplit);
-  cascade_partition(num_decode, hq, hkv, prefix_len, device_num_sms(), part_p, nsplit_p);
+  cascade_partition(num_decode, hq, hkv, prefix_len, device_num_sms(), tc, part_p, nsplit_p);
   return static_cast<size_t>(*nsplit + *nsplit_p) * num_decode * hq * (head_dim + 2) *
          sizeof(float);
 }
@@ -322,8 +322,9 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
     a.cascade = true;
     a.prefix_len = static_cast<int>(plen);
     a.key_begin = a.prefix_len;
+    a.casc_tc = cascade_tc_supported(a);
     decode_need = cascade_workspace(num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
-                                    max_seq_len, a.prefix_len, &a.part, &a.nsplit,
+                                    max_seq_len, a.prefix_len, a.casc_tc, &a.part, &a.nsplit,
                                     &a.part_prefix, &a.nsplit_prefix);
     a.split0 = a.nsplit_prefix;
   } else if (num_decode_seqs > 0 && max_seq_len > 0) {
@@ -509,9 +510,14 @@ size_t pa_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
   const int64_t plen = static_cast<int64_t>(prefix_blocks) * block_size;
   if (prefix_blocks <= 0 || block_size <= 0 || plen >= max_seq_len)
     return pa_attention_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len);
-  return kWorkspaceHeader + cascade_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                              max_seq_len, static_cast<int>(plen), &part, &nsplit,
-                                              &part_p, &nsplit_p);
+  // either prefix pass may run (it depends on the pointers' alignment too)
+  const size_t tc = cascade_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                      static_cast<int>(plen), true, &part, &nsplit, &part_p,
+                                      &nsplit_p);
+  const size_t mma = cascade_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                       max_seq_len, static_cast<int>(plen), false, &part, &nsplit,
+                                       &part_p, &nsplit_p);
+  return kWorkspaceHeader + (tc > mma ? tc : mma);
 }
 
 int pa_attention_cascade(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,

@@ -272,8 +272,36 @@ cudaError_t launch_cascade_d(const AttnArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-void cascade_partition(int num_decode, int hq, int hkv, int prefix_len, int num_sms,
+void cascade_partition(int num_decode, int hq, int hkv, int prefix_len, int num_sms, bool tc,
                        int* part_prefix, int* nsplit_prefix) {
+  if (tc) {
+    // Tensor-core pass: items of (kv head, pair of 128-row tiles, chunk) on a
+    // persistent grid of one CTA per SM.  Chunks are whole 128-key tiles; take
+    // the count with the shortest estimated makespan (waves of items times
+    // tiles per item plus about 1.5 tiles of per-item cost, and a little per
+    // chunk for the merge).
+    const int group = hkv > 0 ? hq / hkv : 1;
+    const int64_t tiles =
+        (static_cast<int64_t>(num_decode) * group + 127) / 128;
+    const int64_t pairs = static_cast<int64_t>(hkv) * ((tiles + 1) / 2);
+    const int ktiles = (prefix_len + 127) / 128;
+    const int sms = num_sms > 0 ? num_sms : 1;
+    int best = 1;
+    double best_t = 1e300;
+    for (int n = 1; n <= ktiles && n <= 256; ++n) {
+      const int per = (ktiles + n - 1) / n;
+      const int64_t items = pairs * ((ktiles + per - 1) / per);
+      const double t = static_cast<double>((items + sms - 1) / sms) * (per + 1.5) + 0.05 * n;
+      if (t < best_t - 1e-9) {
+        best_t = t;
+        best = n;
+      }
+    }
+    const int per = (ktiles + best - 1) / best;
+    *part_prefix = per * 128;
+    *nsplit_prefix = prefix_len > 0 ? (prefix_len + *part_prefix - 1) / *part_prefix : 0;
+    return;
+  }
   // Chunks of at least 256 keys.  Among the chunk counts that give at least
   // one full wave of CTAs (two per SM), take the one whose last wave is
   // fullest, with a small charge per chunk (each adds a partial per row to
@@ -305,6 +333,7 @@ void cascade_partition(int num_decode, int hq, int hkv, int prefix_len, int num_
 
 cudaError_t launch_cascade_prefix(const AttnArgs& a, cudaStream_t st) {
   if (a.num_decode <= 0 || a.nsplit_prefix <= 0) return cudaSuccess;
+  if (a.casc_tc) return launch_cascade_tc(a, st);
   return a.head_dim == 128 ? launch_cascade_d<128>(a, st) : launch_cascade_d<64>(a, st);
 }
 

@@ -63,6 +63,7 @@ struct AttnArgs {
   // [0, nsplit_prefix); the decode kernel then covers keys [key_begin, L) and
   // writes its partials from slot split0 on; the combine merges them all.
   bool cascade;
+  bool casc_tc;  // the prefix pass runs on the tensor-core prefill kernel
   int key_begin, split0, nsplit_prefix, prefix_len, part_prefix;
   // Launch priority of this call's attention kernels (has_priority false: the
   // stream's own).  A mixed step sets it on both sides: the launch attribute
@@ -113,8 +114,12 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t st);
 // Cascade prefix pass (see AttnArgs::cascade); CTAs and slots from
 // cascade_partition.
 cudaError_t launch_cascade_prefix(const AttnArgs& a, cudaStream_t st);
-void cascade_partition(int num_decode, int hq, int hkv, int prefix_len, int num_sms,
+void cascade_partition(int num_decode, int hq, int hkv, int prefix_len, int num_sms, bool tc,
                        int* part_prefix, int* nsplit_prefix);
+// The prefix pass on the tensor-core prefill kernel (query heads per kv head a
+// multiple of 8 dividing 128, and the prefill kernel's own conditions).
+bool cascade_tc_supported(const AttnArgs& a);
+cudaError_t launch_cascade_tc(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t st);
 
 // Tensor-core (tcgen05) prefill: whether the shapes and the environment allow

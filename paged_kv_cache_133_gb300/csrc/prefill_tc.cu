@@ -154,8 +154,11 @@ struct Item {
 // then the new tokens in 128-position windows starting at c, so that every
 // new-token tile is 128 consecutive input rows.
 __device__ __forceinline__ void tile_keys(const Item& I, int j, bool fused, int& key0,
-                                          int& key_end) {
-  if (fused && j >= I.nh) {
+                                          int& key_end, bool casc = false) {
+  if (casc) {  // a chunk [c, kv_end) of a shared prefix
+    key0 = I.c + j * kN;
+    key_end = min(key0 + kN, I.kv_end);
+  } else if (fused && j >= I.nh) {
     key0 = I.c + (j - I.nh) * kN;
     key_end = min(key0 + kN, I.kv_end);
   } else {
@@ -212,7 +215,39 @@ __device__ bool decode_item(const AttnArgs& a, int e, int pairs, int max_level, 
   return true;
 }
 
-template <int D, bool kFused>
+// Shared-prefix (cascade) prefix pass: slot e -> (kv head, pair of 128-row
+// query tiles, key chunk of the prefix).  Query row r of kv head hk is
+// (decode sequence r / g, query head hk * g + r % g).  Fields: h = the two
+// tiles (h[1] < 0: none), c / kv_end = the chunk's keys, t0 = the chunk's
+// partial slot, qn = the kv head's row count, s = 0 (the prefix blocks are
+// read through the first sequence's table).
+__device__ bool decode_item_casc(const AttnArgs& a, int e, Item& it) {
+  const int rows = a.num_decode * a.group;
+  const int tiles = (rows + kM - 1) / kM;
+  const int tpairs = (tiles + 1) / 2;
+  const int per_hk = tpairs * a.nsplit_prefix;
+  const int hk = e / per_hk;
+  const int rest = e - hk * per_hk;
+  const int tp = rest / a.nsplit_prefix;
+  const int ch = rest - tp * a.nsplit_prefix;
+  const int k_lo = ch * a.part_prefix;
+  const int k_hi = min(a.prefix_len, k_lo + a.part_prefix);
+  if (hk >= a.hkv || k_lo >= k_hi) return false;
+  it.s = 0;
+  it.hk = hk;
+  it.h[0] = 2 * tp;
+  it.h[1] = 2 * tp + 1 < tiles ? 2 * tp + 1 : -1;
+  it.t0 = ch;
+  it.qn = rows;
+  it.c = k_lo;
+  it.i0 = 0;
+  it.kv_end = k_hi;
+  it.nh = 0;
+  it.n = (k_hi - k_lo + kN - 1) / kN;
+  return true;
+}
+
+template <int D, bool kFused, bool kCasc = false>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -299,7 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int e = static_cast<int>(atomicAdd(a.sched, 1u));
           if (e >= total_slots) break;
           bool bad;
-          if (decode_item<kFused>(a, e, pairs, max_level, I, bad)) break;
+          if constexpr (kCasc) {
+            bad = false;
+            if (decode_item_casc(a, e, I)) break;
+          } else {
+            if (decode_item<kFused>(a, e, pairs, max_level, I, bad)) break;
+          }
           if (bad) flag_error(a.err, PA_DEV_BAD_LEN);
         }
         const int slot = it & 1;
@@ -311,13 +351,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it > 0 && !wait(bQFree, it - 1)) break;
         const bool hasB = I.h[1] >= 0;
         mbar_expect_tx(BAR(bQFull), Ly::kTile * (hasB ? 2 : 1));
+        if constexpr (kCasc) {
+          // a tile's rows come g at a time: the g query heads of kv head hk
+          // of one decode token (tm_q is [tokens, heads, D] here, box g heads);
+          // rows past the last sequence read an out-of-range token (zeros)
+          for (int sd = 0; sd < (hasB ? 2 : 1); ++sd) {
+            const uint32_t qdst = base + (sd ? Ly::kQB : Ly::kQA);
+            for (int rb = 0; rb < kM; rb += a.group) {
+              const int seq = (I.h[sd] * kM + rb) / a.group;
+              int t0 = seq < a.num_decode ? __ldg(a.qsl + seq) : a.num_tokens;
+              if (t0 < 0 || t0 >= a.num_tokens) t0 = a.num_tokens;
 #pragma unroll
-        for (int hf = 0; hf < Ly::kHalves; ++hf) {
-          tma_load_2d(base + Ly::kQA + hf * Ly::kHalf, &tm_q, I.h[0] * D + hf * 64, I.t0 + I.i0,
-                      BAR(bQFull));
-          if (hasB)
-            tma_load_2d(base + Ly::kQB + hf * Ly::kHalf, &tm_q, I.h[1] * D + hf * 64,
-                        I.t0 + I.i0, BAR(bQFull));
+              for (int hf = 0; hf < Ly::kHalves; ++hf)
+                tma_load_3d(qdst + hf * Ly::kHalf + rb * 128, &tm_q, hf * 64, I.hk * a.group, t0,
+                            BAR(bQFull));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int hf = 0; hf < Ly::kHalves; ++hf) {
+            tma_load_2d(base + Ly::kQA + hf * Ly::kHalf, &tm_q, I.h[0] * D + hf * 64, I.t0 + I.i0,
+                        BAR(bQFull));
+            if (hasB)
+              tma_load_2d(base + Ly::kQB + hf * Ly::kHalf, &tm_q, I.h[1] * D + hf * 64,
+                          I.t0 + I.i0, BAR(bQFull));
+          }
         }
         q_issued = it + 1;
       }
@@ -405,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < I.n; ++j, ++gt) {
         const int st = gt % nst;
         int key0, key_end;
-        tile_keys(I, j, fused, key0, key_end);
+        tile_keys(I, j, fused, key0, key_end, kCasc);
         const uint32_t stile = stage0 + st * Ly::kTile;
         if (fused && j >= I.nh) {
           // new tokens: input rows t0 + (key0 - c) ..., one 128-row box per half
@@ -563,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!next_item(k, I, true)) break;
       if (side == 1 && I.h[1] < 0) continue;
       const int i = I.i0 + r;
-      const int lim = I.c + i;  // last key position this row sees
+      const int lim = kCasc ? I.kv_end - 1 : I.c + i;  // last key position this row sees
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < I.n; ++j) {
         // S_j ready; its commit also covers this side's earlier products, so
@@ -571,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait(side ? bSB : bSA, gx + j))) break;
         tc_fence_after();
         int key0, key_end;
-        tile_keys(I, j, kFused, key0, key_end);
+        tile_keys(I, j, kFused, key0, key_end, kCasc);
         const bool full = key0 + kN - 1 <= lim && key0 + kN <= key_end;
         uint32_t sr[128];
         tmem_ld128(tS, sr);
@@ -664,6 +722,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(BAR(side ? bOFreeB : bOFreeA));
+      if constexpr (kCasc) {
+        // this query row's partial over the chunk: unnormalised O, its
+        // reference m (log2 domain) and sum l, in the chunk's slot
+        const int row = I.h[side] * kM + r;
+        if (row < I.qn) {
+          const int seq = row / a.group;
+          const int head = I.hk * a.group + (row - seq * a.group);
+          const int64_t wr = (static_cast<int64_t>(I.t0) * a.num_decode + seq) * a.hq + head;
+          float4* dst = reinterpret_cast<float4*>(a.ws_o + wr * D);
+#pragma unroll
+          for (int c4 = 0; c4 < D / 4; ++c4)
+            dst[c4] = make_float4(__uint_as_float(o[4 * c4]), __uint_as_float(o[4 * c4 + 1]),
+                                  __uint_as_float(o[4 * c4 + 2]), __uint_as_float(o[4 * c4 + 3]));
+          a.ws_ml[wr * 2] = m_used;
+          a.ws_ml[wr * 2 + 1] = l;
+        }
+        gx += I.n;
+        ++ix;
+        continue;
+      }
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
       for (int e2 = 0; e2 < D / 2; ++e2)
@@ -782,6 +860,22 @@ bool encode_out(CUtensorMap* m, const AttnArgs& a) {
            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q as [tokens, heads, D] with boxes of g heads of one token: the g query
+// heads of a kv head, one decode token (cascade prefix pass).
+bool encode_q_casc(CUtensorMap* m, const AttnArgs& a) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.head_dim), static_cast<cuuint64_t>(a.hq),
+                              static_cast<cuuint64_t>(a.num_tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.head_dim) * 2,
+                                 static_cast<cuuint64_t>(a.q_stride) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(a.group), 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The new tokens' K or V ([T, Hkv, D], token stride in elements): 128-row boxes.
 bool encode_new(CUtensorMap* m, const void* ptr, int64_t stride, const AttnArgs& a) {
   EncodeTiledFn f = encode_fn();
@@ -838,7 +932,56 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+int64_t cascade_tc_slots(const AttnArgs& a) {
+  const int64_t tiles = (static_cast<int64_t>(a.num_decode) * a.group + kM - 1) / kM;
+  return static_cast<int64_t>(a.hkv) * ((tiles + 1) / 2) * a.nsplit_prefix;
+}
+
+template <int D>
+cudaError_t launch_casc_d(const AttnArgs& a, cudaStream_t st) {
+  using Ly = PpLayout<D>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, false, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  CUtensorMap mq, mk, mv, mo, mkn, mvn;
+  memset(&mkn, 0, sizeof(mkn));
+  memset(&mvn, 0, sizeof(mvn));
+  if (!encode_q_casc(&mq, a) || !encode_cache(&mk, a.k_cache, a) ||
+      !encode_cache(&mv, a.v_cache, a) || !encode_out(&mo, a))
+    return cudaErrorNotSupported;
+  const int total = static_cast<int>(cascade_tc_slots(a));
+  const int sms = device_num_sms();
+  const int grid = total < sms ? total : sms;
+  if (grid <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  e = launch_prio(prefill_tc_kernel<D, false, true>, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
+                  a.has_priority, a.priority, mq, mk, mv, mo, mkn, mvn, a, total, 1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace
+
+bool cascade_tc_supported(const AttnArgs& a) {
+  const char* env = getenv("PA_CASCADE_IMPL");
+  if (env && strcmp(env, "mma") == 0) return false;
+  // a kv head's g query heads of one token fill whole 8-row swizzle atoms
+  if (a.group % 8 != 0 || a.group > kM || kM % a.group != 0) return false;
+  if (static_cast<int64_t>(a.num_decode) * a.group > INT_MAX / 4) return false;
+  return prefill_tc_supported(a);
+}
+
+cudaError_t launch_cascade_tc(const AttnArgs& a, cudaStream_t st) {
+  if (a.num_decode <= 0 || a.nsplit_prefix <= 0) return cudaSuccess;
+  return a.head_dim == 128 ? launch_casc_d<128>(a, st) : launch_casc_d<64>(a, st);
+}
 
 bool prefill_tc_supported(const AttnArgs& a) {
   const char* env = getenv("PA_PREFILL_IMPL");

@@ -37,15 +37,20 @@ def _shared(name, num_seqs, prompt, tail_max, hq, hkv, d, bs, seed):
 
 
 def _cases():
+    # Prompts fill whole blocks: the copy-on-write of the last prompt block
+    # then carries prompt tokens only, and every tail starts in a block of its
+    # own (a partial last block would carry the owner's tail into the copies).
     return [
-        # (layout, prefix blocks = the prompt's blocks before the copied last one)
-        _shared("g8_d128_bs16", 6, 700, 60, 16, 2, 128, 16, 1),
-        _shared("g1_d128_bs16", 9, 500, 40, 8, 8, 128, 16, 2),
-        _shared("g4_d64_bs8", 5, 333, 90, 8, 2, 64, 8, 3),
-        _shared("g8_rows_over_64", 20, 260, 30, 16, 2, 128, 16, 4),     # 160 rows per kv head
-        _shared("g16_d128_bs64", 3, 1500, 200, 32, 2, 128, 64, 5),
+        # (layout; prefix blocks = the prompt's blocks before the copied last one)
+        _shared("g8_d128_bs16", 6, 704, 60, 16, 2, 128, 16, 1),
+        _shared("g1_d128_bs16", 9, 512, 40, 8, 8, 128, 16, 2),
+        _shared("g4_d64_bs8", 5, 336, 90, 8, 2, 64, 8, 3),
+        _shared("g8_rows_over_64", 20, 256, 30, 16, 2, 128, 16, 4),     # 160 rows per kv head
+        _shared("g16_d128_bs64", 3, 1536, 200, 32, 2, 128, 64, 5),
         _shared("g2_d128_bs1", 4, 90, 20, 4, 2, 128, 1, 6),
         _shared("long_prefix", 4, 6000, 100, 16, 2, 128, 16, 7),       # several prefix chunks
+        _shared("g8_d64_bs16", 7, 896, 50, 16, 2, 64, 16, 8),
+        _shared("g32_d128_bs32", 3, 416, 30, 32, 1, 128, 32, 9),
     ]
 
 
@@ -99,6 +104,23 @@ def test_cascade_agrees_with_plain_attention(lay):
     assert int(err.item()) == 0
     H.assert_close(H.f64(out_c), H.f64(plain), f"cascade vs plain/{lay.name}")
     assert torch.equal(zero.view(torch.int16), plain.view(torch.int16))
+
+
+@pytest.mark.parametrize("lay", [c for c in _cases() if c.num_q_heads // c.num_kv_heads % 8 == 0],
+                         ids=lambda l: l.name)
+def test_cascade_tensor_core_and_mma_passes_agree(lay, monkeypatch):
+    # query heads per kv head a multiple of 8: the prefix pass runs on the
+    # tensor-core kernel; PA_CASCADE_IMPL=mma forces the mma.sync pass
+    pb = _prefix_blocks(lay)
+    g = workloads.make_tensors(lay, seed=8, device=DEV)
+    md = H.device_meta(lay, DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out_tc = _run(lay, g, md, pb, err).clone()
+    monkeypatch.setenv("PA_CASCADE_IMPL", "mma")
+    out_mma = _run(lay, g, md, pb, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    H.assert_close(H.f64(out_tc), H.f64(out_mma), f"tc vs mma/{lay.name}")
 
 
 def test_cascade_full_size_shared_workload_sampled():
