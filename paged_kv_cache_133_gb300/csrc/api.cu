@@ -122,7 +122,10 @@ static size_t cascade_workspace(int num_decode, int hq, int hkv, int head_dim, i
     return 0;
   const int group = hq / hkv;
   const int units = hkv * ((group + 15) / 16);
-  decode_partition(num_decode, units, max_seq_len - prefix_len, device_num_sms(), part, nsplit);
+  // the own keys run after the prefix pass has filled the GPU: about one wave
+  // of CTAs (a quarter of the SMs' worth of the usual split target)
+  decode_partition(num_decode, units, max_seq_len - prefix_len, (device_num_sms() + 3) / 4, part,
+                   nsplit);
   cascade_partition(num_decode, hq, hkv, prefix_len, device_num_sms(), tc, part_p, nsplit_p);
   return static_cast<size_t>(*nsplit + *nsplit_p) * num_decode * hq * (head_dim + 2) *
          sizeof(float);

@@ -209,6 +209,10 @@ def shared_prefix_layout(seed: int = 0, num_seqs=64, prompt=16384, tail_max=256,
                          num_blocks=4096) -> Layout:
     """Parallel sampling over one shared prompt, with copy-on-write of its last block.
 
+    ``prompt`` should fill whole blocks: the tails are history that each
+    sequence wrote after its copy, so a partial last prompt block would put
+    the owner's tail tokens into the other sequences' copies.
+
     All sequences share the prompt's blocks (ref count ``num_seqs``).  Each one
     then writes into the last prompt block: sequences 0..n-2 move onto fresh
     private copies (one copy pair each), the last one keeps the original, whose
