@@ -79,3 +79,43 @@ def test_graph_replay_matches_eager(lay, fused):
     assert torch.equal(g["k_cache"].view(torch.int16), kc1.view(torch.int16))
     assert torch.equal(g["v_cache"].view(torch.int16), vc1.view(torch.int16))
     assert np.isfinite(H.f64(replay)).all()
+
+
+@pytest.mark.parametrize("g8", [True, False], ids=["tensor_core_prefix", "mma_prefix"])
+def test_cascade_graph_replay_matches_eager(g8):
+    # shared-prompt decode: prefix pass, own keys and combine in one capture
+    hq, hkv = (16, 2) if g8 else (8, 4)
+    lay = workloads.shared_prefix_layout(3, num_seqs=5, prompt=640, tail_max=40, num_q_heads=hq,
+                                         num_kv_heads=hkv, head_dim=128, block_size=16,
+                                         num_blocks=120)
+    tabs = [list(t) for t in lay.tables]
+    pb = 0
+    while all(len(t) > pb for t in tabs) and len({t[pb] for t in tabs}) == 1:
+        pb += 1
+    g = workloads.make_tensors(lay, seed=12, device=DEV)
+    md = H.device_meta(lay, DEV)
+    need = pa.cascade_workspace_size(lay.num_seqs, hq, hkv, 128, lay.max_seq_len, pb,
+                                     lay.block_size)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def step(out):
+        pa.attention_cascade(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"],
+                             md["bt"], prefix_blocks=pb, max_seq_len=lay.max_seq_len,
+                             scale=lay.scale, out=out, workspace=ws, err=err)
+
+    eager = torch.empty_like(g["q"])
+    step(eager)
+    torch.cuda.synchronize()
+    replay = torch.full_like(g["q"], float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(replay)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(replay.view(torch.int16), eager.view(torch.int16))
