@@ -146,6 +146,8 @@ constexpr int kRingOffset = 8 * 32;  // bytes after the barriers (TMEM slot + fl
 struct Item {
   int s, hk, h[2], t0, qn, c, i0, kv_end, n;  // h[1] < 0: no second tile
   int nh;  // fused scatter: tiles of cached history before the new-token tiles (else 0)
+  int pk;  // packed: a tile of <= 64 query tokens holds two heads (rows 0-63: head
+           // h, rows 64-127: head h + 1), so the item covers four heads
 };
 
 // Key range [key0, key_end) of tile j of an item.  Without the fused scatter
@@ -196,10 +198,20 @@ __device__ bool decode_item(const AttnArgs& a, int e, int pairs, int max_level, 
   const int level = max_level - z;
   const int tile = level - 1 - (L - qn + kN - 1) / kN;
   if (tile < 0 || tile >= (qn + kM - 1) / kM) return false;
+  // A tile of at most 64 tokens takes two heads per side (when the group
+  // splits into fours): half the products for the same rows.
+  const bool pk = qn - tile * kM <= kM / 2 && a.group % 4 == 0;
+  if (pk && 4 * p >= a.group) return false;
   it.s = s;
   it.hk = hk;
-  it.h[0] = hk * a.group + 2 * p;
-  it.h[1] = 2 * p + 1 < a.group ? it.h[0] + 1 : -1;
+  it.pk = pk ? 1 : 0;
+  if (pk) {
+    it.h[0] = hk * a.group + 4 * p;
+    it.h[1] = it.h[0] + 2;
+  } else {
+    it.h[0] = hk * a.group + 2 * p;
+    it.h[1] = 2 * p + 1 < a.group ? it.h[0] + 1 : -1;
+  }
   it.t0 = t0;
   it.qn = qn;
   it.c = L - qn;
@@ -243,6 +255,7 @@ __device__ bool decode_item_casc(const AttnArgs& a, int e, Item& it) {
   it.i0 = 0;
   it.kv_end = k_hi;
   it.nh = 0;
+  it.pk = 0;
   it.n = (k_hi - k_lo + kN - 1) / kN;
   return true;
 }
@@ -254,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_o,
                       const __grid_constant__ CUtensorMap tm_kn,
-                      const __grid_constant__ CUtensorMap tm_vn, const AttnArgs a,
+                      const __grid_constant__ CUtensorMap tm_vn,
+                      const __grid_constant__ CUtensorMap tm_q64, const AttnArgs a,
                       int total_slots, int max_level) {
   using Ly = PpLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -293,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_kn);
       prefetch_tmap(&tm_vn);
     }
+    if (!kCasc) prefetch_tmap(&tm_q64);
   }
   tc_fence_before();
   __syncthreads();
@@ -367,6 +382,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             BAR(bQFull));
             }
           }
+        } else if (I.pk) {
+          // two heads per side, 64 rows each (tm_q64: 64-row boxes)
+#pragma unroll
+          for (int hf = 0; hf < Ly::kHalves; ++hf)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              tma_load_2d(base + Ly::kQA + hf * Ly::kHalf + u * (kM / 2) * 128, &tm_q64,
+                          (I.h[0] + u) * D + hf * 64, I.t0 + I.i0, BAR(bQFull));
+              tma_load_2d(base + Ly::kQB + hf * Ly::kHalf + u * (kM / 2) * 128, &tm_q64,
+                          (I.h[1] + u) * D + hf * 64, I.t0 + I.i0, BAR(bQFull));
+            }
         } else {
 #pragma unroll
           for (int hf = 0; hf < Ly::kHalves; ++hf) {
@@ -620,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item I;
       if (!next_item(k, I, true)) break;
       if (side == 1 && I.h[1] < 0) continue;
-      const int i = I.i0 + r;
+      const int i = I.i0 + (I.pk ? (r & (kM / 2 - 1)) : r);  // this row's query token
       const int lim = kCasc ? I.kv_end - 1 : I.c + i;  // last key position this row sees
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < I.n; ++j) {
@@ -748,10 +774,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         o[e2] = pack_bf16(__uint_as_float(o[2 * e2]) * inv, __uint_as_float(o[2 * e2 + 1]) * inv);
       uint8_t* stg = sgen + Ly::kStage + warp * 4096;
       const uint32_t stg_s = base + Ly::kStage + warp * 4096;
-      const int wrow0 = I.i0 + (warp & 3) * 32;  // query row of this warp's lane 0
+      // query token of this warp's lane 0, and its head (packed: warps 0-1
+      // hold the first head's 64 tokens, warps 2-3 the second's)
+      const int wrow0 = I.i0 + (I.pk ? (warp & 1) * 32 : (warp & 3) * 32);
+      const int whead = I.h[side] + (I.pk ? ((warp & 3) >> 1) : 0);
       const bool whole = wrow0 + 32 <= I.qn;
       __nv_bfloat16* ohead = static_cast<__nv_bfloat16*>(a.out) +
-                             static_cast<int64_t>(I.h[side]) * D;
+                             static_cast<int64_t>(whead) * D;
 #pragma unroll
       for (int hh = 0; hh < D / 64; ++hh) {
         if (lane == 0) bulk_wait_read();  // the previous store has read the staging buffer
@@ -765,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tm_o, stg_s, I.h[side] * D + hh * 64, I.t0 + wrow0);
+            tma_store_2d(&tm_o, stg_s, whead * D + hh * 64, I.t0 + wrow0);
             bulk_commit();
           }
         } else {
@@ -819,13 +848,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool encode_q(CUtensorMap* m, const AttnArgs& a) {
+bool encode_q(CUtensorMap* m, const AttnArgs& a, int rows = kM) {
   EncodeTiledFn f = encode_fn();
   if (!f) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.hq) * a.head_dim,
                               static_cast<cuuint64_t>(a.num_tokens)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.q_stride) * 2};
-  const cuuint32_t box[2] = {64, kM};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(rows)};
   const cuuint32_t es[2] = {1, 1};
   return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -910,11 +939,11 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  CUtensorMap mq, mk, mv, mo, mkn, mvn;
+  CUtensorMap mq, mk, mv, mo, mkn, mvn, mq64;
   memset(&mkn, 0, sizeof(mkn));  // unused without the fused scatter
   memset(&mvn, 0, sizeof(mvn));
-  if (!encode_q(&mq, a) || !encode_cache(&mk, a.k_cache, a) || !encode_cache(&mv, a.v_cache, a) ||
-      !encode_out(&mo, a) ||
+  if (!encode_q(&mq, a) || !encode_q(&mq64, a, kM / 2) || !encode_cache(&mk, a.k_cache, a) ||
+      !encode_cache(&mv, a.v_cache, a) || !encode_out(&mo, a) ||
       (a.k_new && (!encode_new(&mkn, a.k_new, a.kn_stride, a) ||
                    !encode_new(&mvn, a.v_new, a.vn_stride, a))))
     return cudaErrorNotSupported;  // nothing launched: the caller takes the general kernel
@@ -928,7 +957,7 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   count_launch();
   const int max_level = max_level_of(a);
   e = launch_prio(prefill_tc_kernel<D, kFused>, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
-                  a.has_priority, a.priority, mq, mk, mv, mo, mkn, mvn, a, total, max_level);
+                  a.has_priority, a.priority, mq, mk, mv, mo, mkn, mvn, mq64, a, total, max_level);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -949,9 +978,10 @@ cudaError_t launch_casc_d(const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  CUtensorMap mq, mk, mv, mo, mkn, mvn;
+  CUtensorMap mq, mk, mv, mo, mkn, mvn, mq64;
   memset(&mkn, 0, sizeof(mkn));
   memset(&mvn, 0, sizeof(mvn));
+  memset(&mq64, 0, sizeof(mq64));  // no packed tiles in this mode
   if (!encode_q_casc(&mq, a) || !encode_cache(&mk, a.k_cache, a) ||
       !encode_cache(&mv, a.v_cache, a) || !encode_out(&mo, a))
     return cudaErrorNotSupported;
@@ -963,7 +993,7 @@ cudaError_t launch_casc_d(const AttnArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   count_launch();
   e = launch_prio(prefill_tc_kernel<D, false, true>, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
-                  a.has_priority, a.priority, mq, mk, mv, mo, mkn, mvn, a, total, 1);
+                  a.has_priority, a.priority, mq, mk, mv, mo, mkn, mvn, mq64, a, total, 1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
