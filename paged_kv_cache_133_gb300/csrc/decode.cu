@@ -410,18 +410,36 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   if (n <= 1) return;
   const int64_t stride = static_cast<int64_t>(a.num_decode) * a.hq;
   const int64_t row0 = static_cast<int64_t>(s) * a.hq + h;
-  float M = -INFINITY;
-  for (int j = 0; j < n; ++j) M = fmaxf(M, a.ws_ml[(row0 + j * stride) * 2]);
-  float lsum = 0.f;
+  // One pass with a running maximum, four partials at a time so that their
+  // loads are in flight together (the merge is exact in any order).
+  float M = -INFINITY, lsum = 0.f;
   float acc[D / 32];
 #pragma unroll
   for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
-  for (int j = 0; j < n; ++j) {
-    const int64_t row = row0 + j * stride;
-    const float w = ex2(a.ws_ml[row * 2] - M);
-    lsum += w * a.ws_ml[row * 2 + 1];
+  for (int j0 = 0; j0 < n; j0 += 4) {
+    float mj[4], lj[4], oj[4][D / 32];
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) acc[i] += w * a.ws_o[row * D + lane + 32 * i];
+    for (int u = 0; u < 4; ++u) {
+      const bool live = j0 + u < n;
+      const int64_t row = row0 + static_cast<int64_t>(live ? j0 + u : j0) * stride;
+      mj[u] = live ? a.ws_ml[row * 2] : -INFINITY;
+      lj[u] = live ? a.ws_ml[row * 2 + 1] : 0.f;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) oj[u][i] = live ? a.ws_o[row * D + lane + 32 * i] : 0.f;
+    }
+    const float Mn = fmaxf(fmaxf(M, fmaxf(mj[0], mj[1])), fmaxf(mj[2], mj[3]));
+    const float c = M == -INFINITY ? 0.f : ex2(M - Mn);
+    lsum *= c;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) acc[i] *= c;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = mj[u] == -INFINITY ? 0.f : ex2(mj[u] - Mn);
+      lsum += w * lj[u];
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) acc[i] += w * oj[u][i];
+    }
+    M = Mn;
   }
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + static_cast<int64_t>(t0) * a.out_stride +
                        static_cast<int64_t>(h) * D;
