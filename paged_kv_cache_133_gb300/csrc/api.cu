@@ -413,7 +413,36 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
       return PA_OK;
     }
   }
-  if (a.cascade) {  // prefix partials, then the own keys and the combine
+  if (a.cascade) {
+    // The prefix pass and each sequence's own keys write disjoint partial
+    // slots: run them side by side (the persistent prefix kernel on the
+    // high-priority side stream, the own keys on the low-priority one) and
+    // join before the combine, which launch_decode queues after them.
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream* side = a.casc_tc ? side_stream() : nullptr;
+    if (side) {
+      if (cudaEventRecord(side->fork, st) != cudaSuccess ||
+          cudaStreamWaitEvent(side->hi, side->fork, 0) != cudaSuccess ||
+          cudaStreamWaitEvent(side->lo, side->fork, 0) != cudaSuccess)
+        return cuda_status(cudaGetLastError());
+      AttnArgs ap = a;
+      ap.has_priority = true;
+      ap.priority = side->greatest;
+      int rc = cuda_status(launch_cascade_prefix(ap, side->hi));
+      if (rc != PA_OK) return rc;
+      AttnArgs ad = a;
+      ad.has_priority = true;
+      ad.priority = side->least;
+      ad.defer_combine = true;
+      rc = cuda_status(launch_decode(ad, side->lo));
+      if (rc != PA_OK) return rc;
+      if (cudaEventRecord(side->join_hi, side->hi) != cudaSuccess ||
+          cudaEventRecord(side->join_lo, side->lo) != cudaSuccess ||
+          cudaStreamWaitEvent(st, side->join_hi, 0) != cudaSuccess ||
+          cudaStreamWaitEvent(st, side->join_lo, 0) != cudaSuccess)
+        return cuda_status(cudaGetLastError());
+      return cuda_status(launch_combine(a, st));
+    }
     int rc = cuda_status(launch_cascade_prefix(a, st));
     if (rc != PA_OK) return rc;
   }

@@ -447,6 +447,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   for (int i = 0; i < D / 32; ++i) out[lane + 32 * i] = __float2bfloat16_rn(acc[i] / lsum);
 }
 
+template <int D>
+cudaError_t launch_combine_d(const AttnArgs& a, cudaStream_t st) {
+  count_launch();
+  cudaError_t e = launch_prio(combine_kernel<D>, dim3(a.num_decode, (a.hq + 3) / 4), dim3(128), 0,
+                              st, a.has_priority, a.priority, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 constexpr int kStages = 3;
 constexpr int kStages8 = 4;  // 8-bit stages are half the bytes: one more in flight
 
@@ -469,11 +477,8 @@ cudaError_t launch_decode_d(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e = launch_prio(decode_kernel<D, kSt, kFp8>, grid, dim3(kThreads), Ly::kBytes, st,
                               a.has_priority, a.priority, a);
   if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess || (a.nsplit <= 1 && !a.cascade)) return e;
-  count_launch();
-  e = launch_prio(combine_kernel<D>, dim3(a.num_decode, (a.hq + 3) / 4), dim3(128), 0, st,
-                  a.has_priority, a.priority, a);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  if (e != cudaSuccess || (a.nsplit <= 1 && !a.cascade) || a.defer_combine) return e;
+  return launch_combine_d<D>(a, st);
 }
 
 }  // namespace
@@ -494,6 +499,11 @@ void decode_partition(int num_decode, int hkv_units, int max_seq_len, int num_sm
   *part = p;
   *nsplit = (max_seq_len + p - 1) / p;
   if (*nsplit < 1) *nsplit = 1;
+}
+
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t st) {
+  if (a.num_decode <= 0) return cudaSuccess;
+  return a.head_dim == 128 ? launch_combine_d<128>(a, st) : launch_combine_d<64>(a, st);
 }
 
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t st) {

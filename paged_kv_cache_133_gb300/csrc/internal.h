@@ -63,7 +63,8 @@ struct AttnArgs {
   // [0, nsplit_prefix); the decode kernel then covers keys [key_begin, L) and
   // writes its partials from slot split0 on; the combine merges them all.
   bool cascade;
-  bool casc_tc;  // the prefix pass runs on the tensor-core prefill kernel
+  bool casc_tc;        // the prefix pass runs on the tensor-core prefill kernel
+  bool defer_combine;  // launch_decode leaves the combine to launch_combine
   int key_begin, split0, nsplit_prefix, prefix_len, part_prefix;
   // Launch priority of this call's attention kernels (has_priority false: the
   // stream's own).  A mixed step sets it on both sides: the launch attribute
@@ -111,6 +112,8 @@ cudaError_t launch_swap_blocks(const void* sk, const void* sv, void* dk, void* d
                                const int32_t* pairs, int n, int src_blocks, int dst_blocks,
                                int block_elems, uint32_t* err, cudaStream_t st);
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t st);
+// The split combine alone (after a launch_decode with defer_combine).
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t st);
 // Cascade prefix pass (see AttnArgs::cascade); CTAs and slots from
 // cascade_partition.
 cudaError_t launch_cascade_prefix(const AttnArgs& a, cudaStream_t st);
