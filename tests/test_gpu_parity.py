@@ -48,6 +48,10 @@ def _small_cases():
         ("d128_bs64_g32", 32, 1, 128, 64, 2, 2),
         ("d64_bs256", 2, 2, 64, 256, 2, 2),
         ("d128_bs128_g6", 12, 2, 128, 128, 3, 3),
+        # short chunks with a group of 4 or 8: tiles of <= 64 tokens carry two
+        # heads per side on the tensor-core kernel
+        ("d64_bs16_g4_short", 8, 2, 64, 16, 2, 5),
+        ("d128_bs16_g8_short", 16, 2, 128, 16, 1, 6),
     ]
     for i, (name, hq, hkv, d, bs, nd, npf) in enumerate(specs):
         cached = list(rng.integers(0, 300, nd)) + list(rng.integers(0, 200, npf))
