@@ -559,7 +559,52 @@ def secondary(dev, steps, warmup, peaks):
                     "additive_roofline_ms": t_star * 1e3, "frac": t_star * 1e3 / ms}
     del st
     res["swap"] = swap_leg(dev)
+    res["kv_copy"] = kv_copy_leg(dev, peaks)
     return res
+
+
+def kv_copy_leg(dev, peaks, launches=200):
+    """The scatter (prefill batch: 8192 tokens) and the copy-on-write copy
+    (shared-prefix batch: 63 block pairs) alone, in GB/s of bytes read plus
+    written, against the measured copy peak."""
+    import torch
+    import paged_kv_cache_133_gb300 as pa
+    out = {}
+    lay = workloads.config_layout(3, 0)
+    st = Step(lay, dev)
+    g, md = st.g, st.md
+    nbytes = 2 * 2 * g["k"].numel() * g["k"].element_size()  # K and V, read + written
+
+    def scatter():
+        pa.write_kv(g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"], err=st.err)
+
+    lay5 = workloads.config_layout(5, 0)
+    st5 = Step(lay5, dev)
+    g5, md5 = st5.g, st5.md
+    pair_bytes = 2 * 2 * lay5.block_size * lay5.num_kv_heads * lay5.head_dim * 2
+    cbytes = len(lay5.cow_pairs) * pair_bytes
+
+    def copy():
+        pa.copy_blocks(g5["k_cache"], g5["v_cache"], md5["pairs"], err=st5.err)
+
+    for name, fn, b, what in (("scatter", scatter, nbytes, "8192 tokens x 2 KB of K and of V"),
+                              ("copy_blocks", copy, cbytes, "63 pairs x 64 KB of K+V")):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(launches):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(e) * 1e3 / launches
+        gbs = b / (us * 1e-6) / 1e9
+        out[name] = {"what": what, "bytes_read_plus_written": b, "us_per_launch": us, "GB/s": gbs,
+                     "of_copy_peak": gbs / peaks["hbm"],
+                     "note": "back-to-back launches; the working set stays in L2 when it fits"}
+    del st, st5
+    return out
 
 
 class Fp8Step:

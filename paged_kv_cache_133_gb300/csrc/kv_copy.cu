@@ -19,29 +19,46 @@ __global__ void __launch_bounds__(256) write_kv_kernel(const uint4* __restrict__
                                                        const int32_t* __restrict__ slots, int T,
                                                        int vec_per_row, int64_t num_slots,
                                                        uint32_t* err) {
-  const int64_t total = static_cast<int64_t>(T) * vec_per_row;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(i / vec_per_row);
-    const int c = static_cast<int>(i - static_cast<int64_t>(t) * vec_per_row);
+  // One warp per token row (grid-stride over tokens), the lanes across the
+  // row's 16-byte pieces: no index division, and each lane's loads of a row
+  // are issued before its stores.
+  const int lane = threadIdx.x & 31;
+  const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+  for (int t = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5); t < T;
+       t += nwarps) {
     const int slot = __ldg(slots + t);
     if (slot < 0) continue;
     if (slot >= num_slots) {
-      if (c == 0) flag_error(err, PA_DEV_BAD_SLOT);
+      if (lane == 0) flag_error(err, PA_DEV_BAD_SLOT);
       continue;
     }
-    const uint4 kv = __ldg(k + t * ks + c);
-    const uint4 vv = __ldg(v + t * vs + c);
-    const int64_t o = static_cast<int64_t>(slot) * vec_per_row + c;
-    kc[o] = kv;
-    vc[o] = vv;
+    const uint4* kr = k + static_cast<int64_t>(t) * ks;
+    const uint4* vr = v + static_cast<int64_t>(t) * vs;
+    uint4* kd = kc + static_cast<int64_t>(slot) * vec_per_row;
+    uint4* vd = vc + static_cast<int64_t>(slot) * vec_per_row;
+    int c = lane;
+    for (; c + 96 < vec_per_row; c += 128) {
+      uint4 a[4], b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a[u] = __ldg(kr + c + 32 * u);
+        b[u] = __ldg(vr + c + 32 * u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        kd[c + 32 * u] = a[u];
+        vd[c + 32 * u] = b[u];
+      }
+    }
+    for (; c < vec_per_row; c += 32) {
+      const uint4 a = __ldg(kr + c);
+      const uint4 b = __ldg(vr + c);
+      kd[c] = a;
+      vd[c] = b;
+    }
   }
 }
 
-// The scatter of an 8-bit cache: one thread per 8 elements (16 bytes in, 8
-// bytes out) of a token row.  Each element is multiplied by the reciprocal
-// scale in fp32 and rounded to the nearest E4M3 code, ties to even,
-// saturating at the largest finite magnitude.
 __global__ void __launch_bounds__(256) write_kv_fp8_kernel(const uint4* __restrict__ k,
                                                            const uint4* __restrict__ v, int64_t ks,
                                                            int64_t vs, uint2* __restrict__ kc,
@@ -135,8 +152,7 @@ cudaError_t launch_write_kv(const void* k, const void* v, int64_t ks, int64_t vs
                             int row_elems, uint32_t* err, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int vpr = row_elems / 8;
-  const int64_t total = static_cast<int64_t>(T) * vpr;
-  int64_t blocks = (total + 255) / 256;
+  int64_t blocks = (static_cast<int64_t>(T) + 7) / 8;  // a warp per token, 8 warps per block
   if (blocks > 152 * 16) blocks = 152 * 16;
   count_launch();
   write_kv_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
