@@ -34,6 +34,14 @@
  * lengths) sets PA_DEV_* bits in *err_flag with atomicOr (err_flag may be
  * NULL to skip reporting); the offending rows are skipped and their outputs
  * are unspecified.  No kernel traps and no kernel waits on another block.
+ *
+ * Environment (read at each call; results are unchanged within rounding):
+ *   PA_PREFILL_IMPL=mma    prefill rows on the mma.sync kernel instead of the
+ *                          tcgen05 one.
+ *   PA_CASCADE_IMPL=mma    pa_attention_cascade's prefix pass on the mma.sync
+ *                          kernel instead of the tcgen05 one.
+ *   PA_MIXED_DECODE_SMS=n  SMs left to the decode rows while a mixed step's
+ *                          prefill runs beside them (default 49 % of the SMs).
  */
 #ifndef PA_H_
 #define PA_H_
