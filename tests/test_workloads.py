@@ -102,3 +102,20 @@ def test_poison_marks_only_dead_slots():
                 assert nan
             else:
                 assert not torch.isnan(kc[b, o]).any().item()
+
+
+def test_shared_prefix_blocks_of_the_shared_workload():
+    # the bench's cascade leg passes the leading table entries every sequence
+    # shares: the prompt's blocks before the copied last one
+    import bench
+    lay = workloads.config_layout(5, 0)
+    assert bench.shared_prefix_blocks(lay) == 1023
+    small = workloads.shared_prefix_layout(1, num_seqs=4, prompt=160, tail_max=20,
+                                           num_q_heads=8, num_kv_heads=2, head_dim=64,
+                                           block_size=16, num_blocks=64)
+    assert bench.shared_prefix_blocks(small) == 9
+    # every key position below the shared prefix maps to the same block in every table
+    for s in range(small.num_seqs):
+        assert list(small.tables[s][:9]) == list(small.tables[0][:9])
+    # the copied last prompt block differs for all but the last sequence
+    assert len({int(small.tables[s][9]) for s in range(small.num_seqs)}) == small.num_seqs
