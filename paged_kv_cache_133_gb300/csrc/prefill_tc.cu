@@ -600,6 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           issue_pv(0, g, j > 0);
+          if (!more) mma_commit(BAR(bPvA));  // side A's O products of the item are issued
           if (more) {
             if (!(ok = wait(bKFull0 + (g + 1) % Ly::kKStages, (g + 1) / Ly::kKStages))) break;
             tc_fence_after();
@@ -611,10 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_pv(1, g, j > 0);
             if (more) issue_s(1, g + 1);
           }
-          if (!more) {  // the item's O products are all issued
-            mma_commit(BAR(bPvA));
-            if (hasB) mma_commit(BAR(bPvB));
-          }
+          if (!more && hasB) mma_commit(BAR(bPvB));
           mma_commit(BAR(bVEmpty0 + g % Ly::kVStages));
           if (more) mma_commit(BAR(bKEmpty0 + (g + 1) % Ly::kKStages));
           if (j + 2 == I.n) mma_commit(BAR(bQFree));  // the item's last S products are issued
