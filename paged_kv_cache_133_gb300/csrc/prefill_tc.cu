@@ -18,6 +18,14 @@
 // counter (atomicAdd) whenever its CTA has room, so CTAs that drew cheap
 // items draw more and all finish together.
 //
+// A token tile of at most 64 tokens (the tail of a chunk) is "packed" when
+// the group splits into fours: each side's 128 rows hold two heads (rows
+// 0-63 one head, 64-127 the next), so one item covers four heads with half
+// the products.  A third mode (kCasc) runs the prefix pass of a shared-prefix
+// decode: a side's rows are the (decode token, query head) pairs of a kv
+// head, keys are a chunk of the shared prefix with no causal mask, and the
+// epilogue writes fp32 partials (O, m, l) for the split combine.
+//
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3   softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
 //   warps 4-7   softmax + epilogue of tile B
