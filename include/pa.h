@@ -68,8 +68,9 @@ typedef enum {
                                 q_len > max_query_len or seq_len > max_seq_len     */
 #define PA_DEV_BAD_DECODE 8u /* a row below num_decode_seqs has q_len != 1          */
 #define PA_DEV_BAD_PAIR 16u  /* a copy pair names a block outside the pool          */
-#define PA_DEV_TIMEOUT 32u   /* a pipeline wait inside a kernel ran out of time (2 s);
-                                the kernel drained and exited, outputs unspecified   */
+#define PA_DEV_TIMEOUT 32u   /* a pipeline wait inside a kernel ran out of time (2 s,
+                                or pa_set_wait_limit_ns); the kernel drained its
+                                copies and products and exited, outputs unspecified */
 
 /*
  * pa_write_kv — scatter the new tokens' K and V into the paged cache.
@@ -236,10 +237,11 @@ int pa_write_kv_fp8(const void* k, const void* v, int64_t k_stride_t, int64_t v_
  * pa_attention_fp8 — pa_attention over an 8-bit cache, for decode steps:
  * every sequence must be a decode row (num_decode_seqs == num_seqs, else
  * PA_ERR_UNSUPPORTED; the tensor-core prefill reads bf16 only).  Keys and
- * values are the codes times k_scale / v_scale.  The kernel widens each
- * 16-token group to fp16 (exact for every code) and runs the products in
- * fp16 with fp32 accumulation; q is converted to fp16 once, so |q| must stay
- * below 65504.  Workspace and errors as pa_attention.
+ * values are the codes times k_scale / v_scale.  The kernel stages the codes
+ * in shared memory as they are, converts each mma fragment to fp16 in
+ * registers (exact for every code) and runs the products in fp16 with fp32
+ * accumulation; q is converted to fp16 once, so |q| must stay below 65504.
+ * Workspace and errors as pa_attention.
  */
 int pa_attention_fp8(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,
                      const void* k_cache, const void* v_cache, const int32_t* query_start_loc,
@@ -267,7 +269,8 @@ int pa_attention_fp8(void* out, int64_t out_stride_t, const void* q, int64_t q_s
  *
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.  A
- * failed lookup returns PA_ERR_CUDA without updating pa_last_cuda_error.
+ * failed lookup returns PA_ERR_CUDA and records the CUDA error for
+ * pa_last_cuda_error (the runtime's own last-error state is cleared).
  * Every call shares the array and it keeps the previous call's contents;
  * nothing in it has to start at zero.  Calls that overlap on the GPU (other
  * streams or host threads) race on the array: serialise them.
@@ -329,6 +332,22 @@ int pa_last_cuda_error(void);
 
 /* Number of kernels this library has launched since it was loaded (all threads). */
 uint64_t pa_kernel_launches(void);
+
+/*
+ * pa_set_wait_limit_ns — failure-detection control (not part of the method).
+ *
+ * The tensor-core prefill kernel (also the shared-prefix pass) waits on
+ * shared-memory barriers for its copies and products.  Each such wait gives
+ * up after a limit: the kernel then sets PA_DEV_TIMEOUT in err_flag, waits
+ * for its own copies and products still in flight (each of those drain waits
+ * bounded at 2 s), frees its tensor memory and exits, so that the context
+ * stays usable.  This sets that limit for launches made after the call, for
+ * every thread and device of the process; 0 restores the default of 2 s.  A
+ * short limit makes an ordinary call time out on purpose, which is how a
+ * test checks that the give-up path returns cleanly.  Returns the previous
+ * setting.
+ */
+uint64_t pa_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,7 @@ __all__ = ["write_kv", "attention", "write_kv_attention", "attention_noalloc", "
            "swap_blocks", "write_kv_fp8", "attention_fp8", "attention_cascade", "workspace_size",
            "cascade_workspace_size", "kernel_launches",
            "library_path", "load", "PaError", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN",
-           "DEV_BAD_DECODE", "DEV_BAD_PAIR"]
+           "DEV_BAD_DECODE", "DEV_BAD_PAIR", "DEV_TIMEOUT", "set_wait_limit_ns"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_lib", "libpa133.so")
@@ -32,6 +32,7 @@ DEV_BAD_BLOCK = 2
 DEV_BAD_LEN = 4
 DEV_BAD_DECODE = 8
 DEV_BAD_PAIR = 16
+DEV_TIMEOUT = 32
 
 _c_i = ctypes.c_int
 _c_i64 = ctypes.c_int64
@@ -68,6 +69,7 @@ _SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [_c_i]),
     "pa_last_cuda_error": (_c_i, []),
     "pa_kernel_launches": (ctypes.c_uint64, []),
+    "pa_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
 }
 
 
@@ -150,6 +152,14 @@ def _cache8(t, name):
 
 def kernel_launches() -> int:
     return int(load().pa_kernel_launches())
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of each pipeline wait inside the tensor-core kernels for later
+    launches (0: the default 2 s); returns the previous setting.  A wait that
+    runs out sets ``PA_DEV_TIMEOUT`` in the error flag and the kernel exits
+    cleanly."""
+    return int(load().pa_set_wait_limit_ns(int(ns)))
 
 
 def write_kv(k, v, k_cache, v_cache, slot_mapping, err=None, stream=None):
@@ -416,8 +426,10 @@ def attention_noalloc(q, k_cache, v_cache, query_start_loc, seq_lens, block_tabl
     for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
                  (block_tables, "block_tables")):
         _i32(t, n)
+    _need(block_tables.dim() == 2, "block_tables must be [num_seqs, max_blocks_per_seq]")
     nb, bs, hkv, d = k_cache.shape
-    T, hq, _ = q.shape
+    T, hq, dq = q.shape
+    _need(dq == d, "q head_dim differs from the cache's")
     _need(out.shape == q.shape, "out shape differs from q")
     S = seq_lens.numel()
     _need(query_start_loc.numel() == S + 1 and block_tables.shape[0] == S, "metadata sizes differ")

@@ -13,6 +13,8 @@ namespace pa {
 
 static std::atomic<uint64_t> g_launches{0};
 static thread_local int g_last_cuda_error = 0;
+// Limit of the tensor-core kernels' pipeline waits (pa_set_wait_limit_ns; 0: default)
+static std::atomic<uint64_t> g_wait_ns{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
@@ -88,6 +90,8 @@ static int cuda_status(cudaError_t e) {
   return PA_ERR_CUDA;
 }
 
+int record_cuda_error(cudaError_t e) { return e == cudaSuccess ? PA_OK : cuda_status(e); }
+
 static int ilog2_exact(int x) {
   if (x <= 0 || (x & (x - 1))) return -1;
   int l = 0;
@@ -150,6 +154,8 @@ const char* pa_status_string(int status) {
 }
 
 int pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t pa_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
 
 uint64_t pa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -314,6 +320,7 @@ static int attention_impl(void* out, int64_t out_stride_t, const void* q, int64_
   a.num_blocks = num_blocks;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.err = err_flag;
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   size_t decode_need = 0;

@@ -9,6 +9,10 @@ namespace pa {
 
 void count_launch();
 
+// Records a CUDA error for pa_last_cuda_error on this thread; returns
+// PA_ERR_CUDA (PA_OK for cudaSuccess).
+int record_cuda_error(cudaError_t e);
+
 // SM count of the current device (cached per device).
 int device_num_sms();
 
@@ -71,6 +75,10 @@ struct AttnArgs {
   // is recorded in the kernel node when the step is captured into a CUDA graph.
   bool has_priority;
   int priority;
+  // Limit of each pipeline wait inside the tensor-core kernels, in ns (the
+  // value pa_set_wait_limit_ns set; 0: the default of 2 s).  Their drain
+  // waits on the way out keep the default.
+  uint64_t wait_ns;
 };
 
 // Launches `kernel` on `st` with the given priority as a launch attribute when

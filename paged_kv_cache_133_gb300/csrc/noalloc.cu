@@ -24,6 +24,7 @@
 
 #include <mutex>
 
+#include "internal.h"
 #include "pa.h"
 
 namespace {
@@ -46,7 +47,12 @@ int scratch_address(void** out) {
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return static_cast<int>(e);
+    if (e != cudaSuccess) {
+      // Clear the runtime's last error: a later launch check in another call
+      // must not pick up this failure and report its own launch as failed.
+      cudaGetLastError();
+      return static_cast<int>(e);
+    }
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];
@@ -69,7 +75,8 @@ extern "C" int pa_attention_noalloc(void* out, int64_t out_stride_t, const void*
   if (need > kNoallocScratchBytes) return PA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0) {
-    if (scratch_address(&scratch) != 0) return PA_ERR_CUDA;
+    const int e = scratch_address(&scratch);
+    if (e != 0) return pa::record_cuda_error(static_cast<cudaError_t>(e));
   }
   return pa_attention(out, out_stride_t, q, q_stride_t, k_cache, v_cache, query_start_loc,
                       seq_lens, block_tables, num_seqs, num_tokens, max_blocks_per_seq,

@@ -38,9 +38,10 @@
 // The producers' lanes resolve a tile's blocks through the block table and
 // issue one TMA box each.
 // The softmax warpgroups raise their register limit to 200 and the third
-// warpgroup lowers its to 96 (256*200 + 128*96 = 63488 <= 384*168 launched;
-// per SM sub-partition 200+200+96 registers x 32 lanes <= 16384), so a softmax
-// thread holds its whole 128-score row after one TMEM load.
+// warpgroup lowers its to 104 (256*200 + 128*104 = 64512 = 384*168 launched;
+// per SM sub-partition 200+200+104 registers x 32 lanes <= 16384), so a
+// softmax thread holds its whole 128-score row after one TMEM load and the
+// producer, MMA and scheduler code runs without spills.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // P (bf16, two per 32-bit column) is written over the first 64 columns of its
 // own S and read from there as the A operand of O += P V.  Per key tile j the
@@ -59,9 +60,9 @@
 // result is exact for any m; the threshold only bounds P <= 256.  Scores are in
 // the log2 domain (scale pre-multiplied by log2 e).
 //
-// Every mbarrier wait is bounded (2 s); on expiry the kernel sets
-// PA_DEV_TIMEOUT, drains its in-flight copies and MMAs (bounded), frees TMEM
-// and exits.
+// Every mbarrier wait is bounded (2 s, or the limit pa_set_wait_limit_ns
+// set); on expiry the kernel sets PA_DEV_TIMEOUT, drains its in-flight copies
+// and MMAs (each drain wait bounded at 2 s), frees TMEM and exits.
 #include <cuda.h>
 #include <limits.h>
 #include <math.h>
@@ -128,14 +129,14 @@ struct PpLayout {
   static constexpr int kTile = kHalves * kHalf;  // Q, K or V tile
   static constexpr int kKStages = 2;
   static constexpr int kVStages = 2;
-  static constexpr int kQA = 0;
-  static constexpr int kQB = kTile;
+  static constexpr int kQ = 0;  // Q of side A, then of side B
   static constexpr int kK = 2 * kTile;
   static constexpr int kV = kK + kKStages * kTile;
   static constexpr int kStage = kV + kVStages * kTile;  // output staging, 4 KB per softmax warp
   static constexpr int kBar = kStage + kSoftmaxWarps * 4096;
   static constexpr int kBytes = kBar + 512;  // barriers, TMEM slot, flags, item ring
   static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1 KB
+  __host__ __device__ static constexpr int q(int side) { return kQ + side * kTile; }
 };
 
 enum : int {
@@ -146,9 +147,10 @@ enum : int {
   bItemFull0, bItemFull1, bItemEmpty0, bItemEmpty1, kNumBars
 };
 
-// Threads that take each item from the ring: one lane of the K producer, the
-// MMA and the V producer warps, and every softmax thread.
-constexpr uint32_t kItemReaders = 3 + 256;
+
+// Arrivals that release each item's ring entry: one lane of the K producer,
+// the MMA and the V producer warps, and every softmax thread.
+constexpr uint32_t kItemReaders = 3 + 32 * kSoftmaxWarps;
 constexpr int kRingOffset = 8 * 32;  // bytes after the barriers (TMEM slot + flags first)
 
 struct Item {
@@ -268,7 +270,11 @@ __device__ bool decode_item_casc(const AttnArgs& a, int e, Item& it) {
   return true;
 }
 
-template <int D, bool kFused, bool kCasc = false>
+// kPoll: the instantiation launched when an explicit wait limit is set
+// (pa_set_wait_limit_ns): every wait polls without suspending, so that even a
+// limit of a few nanoseconds holds.  The default instantiation's first probe
+// of a barrier may suspend inside the hardware until the phase completes.
+template <int D, bool kFused, bool kCasc = false, bool kPoll = false>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -328,24 +334,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto wait = [&](int b, int completion) -> bool {
     const uint32_t parity = static_cast<uint32_t>(completion) & 1u;
-    if (mbar_try_wait(BAR(b), parity)) return true;
+    if constexpr (kPoll) {
+      if (mbar_test_wait(BAR(b), parity)) return true;
+    } else {
+      if (mbar_try_wait(BAR(b), parity)) return true;
+    }
     if (*abort_flag) return false;
-    if (mbar_wait(BAR(b), parity, kWaitNs)) return true;
+    if (mbar_wait(BAR(b), parity, a.wait_ns ? a.wait_ns : kWaitNs)) return true;
     give_up();
     return false;
   };
 
-  // Take item number `it` from the ring (every thread of a reading role calls
-  // this; `arrive` is true for the thread that reports the entry consumed).
+  // Waits of the warp-collective roles (softmax, producers).  Under a short
+  // explicit limit (kPoll) one lane's wait can run out while another's sees
+  // the phase complete; the warp then takes the outcome together, so that no
+  // lane is left alone at a warp-wide instruction (tcgen05.ld/st, shuffles,
+  // __syncwarp).  Under the default 2 s limit every lane polls the same phase,
+  // so the lanes give up together unless it completes within the same
+  // microsecond; the waits stay per lane there, without a vote.
+  auto wait_w = [&](int b, int completion) -> bool {
+    if constexpr (kPoll) return __all_sync(0xffffffffu, wait(b, completion));
+    else return wait(b, completion);
+  };
+
+  // Take item number `it` from the ring (every lane of a reading warp calls
+  // this); `arrive`: this thread reports the entry consumed.
   auto next_item = [&](int it, Item& I, bool arrive) -> bool {
     const int slot = it & 1;
-    if (!wait(bItemFull0 + slot, it >> 1)) return false;
+    if (!wait_w(bItemFull0 + slot, it >> 1)) return false;
     I = ring[slot];  // ordered after the acquiring wait (asm with a memory clobber)
     if (arrive) mbar_arrive(BAR(bItemEmpty0 + slot));
     return I.n > 0;
   };
 
-  if (warp >= kProducerWarp) regs_decrease<96>();
+  // The Q boxes of an item.  A packed item has two heads per side in 64-row
+  // boxes (tm_q64).
+  auto q_copy = [&](const Item& I) {
+    const uint32_t full = BAR(bQFull);
+    if (I.pk) {
+#pragma unroll
+      for (int hf = 0; hf < Ly::kHalves; ++hf)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)  // heads h[0], h[0]+1 (side A), h[1], h[1]+1 (side B)
+          tma_load_2d(base + Ly::q(u >> 1) + hf * Ly::kHalf + (u & 1) * (kM / 2) * 128,
+                      &tm_q64, (I.h[u >> 1] + (u & 1)) * D + hf * 64, I.t0 + I.i0, full);
+    } else {
+#pragma unroll
+      for (int hf = 0; hf < Ly::kHalves; ++hf)
+#pragma unroll
+        for (int sd = 0; sd < 2; ++sd)
+          if (sd == 0 || I.h[1] >= 0)
+            tma_load_2d(base + Ly::q(sd) + hf * Ly::kHalf, &tm_q, I.h[sd] * D + hf * 64,
+                        I.t0 + I.i0, full);
+    }
+  };
+
+  if (warp >= kProducerWarp) regs_decrease<104>();
   if (warp == kSchedWarp) {
     // ------------------------------------------------------------ scheduler
     if (lane == 0) {
@@ -379,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // of one decode token (tm_q is [tokens, heads, D] here, box g heads);
           // rows past the last sequence read an out-of-range token (zeros)
           for (int sd = 0; sd < (hasB ? 2 : 1); ++sd) {
-            const uint32_t qdst = base + (sd ? Ly::kQB : Ly::kQA);
+            const uint32_t qdst = base + Ly::q(sd);
             for (int rb = 0; rb < kM; rb += a.group) {
               const int seq = (I.h[sd] * kM + rb) / a.group;
               int t0 = seq < a.num_decode ? __ldg(a.qsl + seq) : a.num_tokens;
@@ -390,30 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             BAR(bQFull));
             }
           }
-        } else if (I.pk) {
-          // two heads per side, 64 rows each (tm_q64: 64-row boxes)
-#pragma unroll
-          for (int hf = 0; hf < Ly::kHalves; ++hf)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              tma_load_2d(base + Ly::kQA + hf * Ly::kHalf + u * (kM / 2) * 128, &tm_q64,
-                          (I.h[0] + u) * D + hf * 64, I.t0 + I.i0, BAR(bQFull));
-              tma_load_2d(base + Ly::kQB + hf * Ly::kHalf + u * (kM / 2) * 128, &tm_q64,
-                          (I.h[1] + u) * D + hf * 64, I.t0 + I.i0, BAR(bQFull));
-            }
         } else {
-#pragma unroll
-          for (int hf = 0; hf < Ly::kHalves; ++hf) {
-            tma_load_2d(base + Ly::kQA + hf * Ly::kHalf, &tm_q, I.h[0] * D + hf * 64, I.t0 + I.i0,
-                        BAR(bQFull));
-            if (hasB)
-              tma_load_2d(base + Ly::kQB + hf * Ly::kHalf, &tm_q, I.h[1] * D + hf * 64,
-                          I.t0 + I.i0, BAR(bQFull));
-          }
+          q_copy(I);
         }
         q_issued = it + 1;
       }
-      // drain: the last Q copy has landed before the CTA exits
+      // drain: the last Q copy has landed before the CTA exits (each earlier
+      // one was consumed before the next was issued)
       if (q_issued > 0) mbar_wait(BAR(bQFull), (q_issued - 1) & 1, kWaitNs);
     }
     __syncwarp();
@@ -446,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Item pend_I{};
     auto scatter = [&]() -> bool {
       const int g = pend_g;
-      if (!wait(full0 + g % nst, g / nst)) return false;
+      if (!wait_w(full0 + g % nst, g / nst)) return false;
       const uint8_t* sg = sgen + (stage0 - base) + (g % nst) * Ly::kTile;
       const Item& P = pend_I;
       const int rows = min(kM, P.qn - P.i0);
@@ -475,9 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto before_refill = [&](int st) -> bool {
       if (pend_g < 0) return true;
       if (st != pend_g % nst) {  // optional: only while the stage is busy and the rows are in
-        const bool busy = gt >= nst && !__all_sync(0xffffffffu, mbar_try_wait(BAR(empty0 + st),
+        const bool busy = gt >= nst && !__all_sync(0xffffffffu, mbar_test_wait(BAR(empty0 + st),
                                                                               (gt / nst - 1) & 1));
-        const bool landed = __all_sync(0xffffffffu, mbar_try_wait(BAR(full0 + pend_g % nst),
+        const bool landed = __all_sync(0xffffffffu, mbar_test_wait(BAR(full0 + pend_g % nst),
                                                                   (pend_g / nst) & 1));
         if (!busy || !landed) return true;
       }
@@ -502,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (fused && j >= I.nh) {
           // new tokens: input rows t0 + (key0 - c) ..., one 128-row box per half
           if (!(ok = before_refill(st))) break;
-          if (gt >= nst && !(ok = wait(empty0 + st, gt / nst - 1))) break;
+          if (gt >= nst && !(ok = wait_w(empty0 + st, gt / nst - 1))) break;
           if (lane == 0) {
             mbar_expect_tx(BAR(full0 + st), kN * 128 * Ly::kHalves);
 #pragma unroll
@@ -527,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t valid = __ballot_sync(0xffffffffu, slot >= 0);
         const uint32_t bytes = static_cast<uint32_t>(__popc(valid) * R * 128 * Ly::kHalves);
         if (!(ok = before_refill(st))) break;
-        if (gt >= nst && !(ok = wait(empty0 + st, gt / nst - 1))) break;
+        if (gt >= nst && !(ok = wait_w(empty0 + st, gt / nst - 1))) break;
         if (lane == 0) mbar_expect_tx(BAR(full0 + st), bytes);
         __syncwarp();
         if (slot >= 0) {
@@ -563,13 +590,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // so each product costs one add per operand.  (The issuing lane shares its
     // sub-partition with two softmax warps, so every instruction it saves
     // shortens the gap between a P being ready and its product starting.)
-    const uint64_t dQA = smem_desc_sw128(base + Ly::kQA, 16, 1024);
-    const uint64_t dQB = smem_desc_sw128(base + Ly::kQB, 16, 1024);
+    const uint64_t dQ0 = smem_desc_sw128(base + Ly::kQ, 16, 1024);
     const uint64_t dK0 = smem_desc_sw128(base + Ly::kK, 16, 1024);
     const uint64_t dV0 = smem_desc_sw128(base + Ly::kV, Ly::kHalf, 1024);
     const uint32_t tS0 = tmem, tO0 = tmem + 256;
+    // S of one side for key tile g
     auto issue_s = [&](int side, int g) {
-      const uint64_t a0 = side ? dQB : dQA;
+      const uint64_t a0 = dQ0 + static_cast<uint64_t>(Ly::q(side) >> 4);
       const uint64_t b0 = dK0 + static_cast<uint64_t>((g % Ly::kKStages) * (Ly::kTile >> 4));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -586,23 +613,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kIdO, (acc || kk > 0) ? 1u : 0u);
     };
     // One lane issues everything; the V rows past the last key of a partial
-    // tile are zeroed by softmax A before it reports its P.
+    // tile are zeroed by softmax A before it reports its P.  This lane needs
+    // only an item's tile count and whether it has a side B.
+    auto next_nb = [&](int it, int& n, bool& hb) -> bool {
+      const int slot = it & 1;
+      if (!wait(bItemFull0 + slot, it >> 1)) return false;
+      n = ring[slot].n;
+      hb = ring[slot].h[1] >= 0;
+      mbar_arrive(BAR(bItemEmpty0 + slot));
+      return n > 0;
+    };
     if (lane == 0) {
       int gt = 0, it = 0, gB = 0, itB = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        Item I;
-        if (!next_item(k, I, true)) break;
-        const bool hasB = I.h[1] >= 0;
+        int n = 0;
+        bool hasB = false;
+        if (!next_nb(k, n, hasB)) break;
         if (!(ok = wait(bQFull, it) && wait(bKFull0 + gt % Ly::kKStages, gt / Ly::kKStages))) break;
         tc_fence_after();
         issue_s(0, gt);
         if (hasB) issue_s(1, gt);
         mma_commit(BAR(bKEmpty0 + gt % Ly::kKStages));
-        if (I.n == 1) mma_commit(BAR(bQFree));
-        for (int j = 0; j < I.n; ++j) {
+        if (n == 1) mma_commit(BAR(bQFree));
+        for (int j = 0; j < n; ++j) {
           const int g = gt + j;
-          const bool more = j + 1 < I.n;
+          const bool more = j + 1 < n;
           ok = wait(bPA, g) && (j > 0 || it == 0 || wait(bOFreeA, it - 1)) &&
                wait(bVFull0 + g % Ly::kVStages, g / Ly::kVStages);
           if (!ok) break;
@@ -623,13 +659,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!more && hasB) mma_commit(BAR(bPvB));
           mma_commit(BAR(bVEmpty0 + g % Ly::kVStages));
           if (more) mma_commit(BAR(bKEmpty0 + (g + 1) % Ly::kKStages));
-          if (j + 2 == I.n) mma_commit(BAR(bQFree));  // the item's last S products are issued
+          if (j + 2 == n) mma_commit(BAR(bQFree));  // the item's last S products are issued
         }
         if (!ok) break;
-        gt += I.n;
+        gt += n;
         ++it;
         if (hasB) {
-          gB += I.n;
+          gB += n;
           ++itB;
         }
       }
@@ -658,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < I.n; ++j) {
         // S_j ready; its commit also covers this side's earlier products, so
         // the P columns and O may be rewritten below.
-        if (!(ok = wait(side ? bSB : bSA, gx + j))) break;
+        if (!(ok = wait_w(side ? bSB : bSA, gx + j))) break;
         tc_fence_after();
         int key0, key_end;
         tile_keys(I, j, kFused, key0, key_end, kCasc);
@@ -721,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
         const int live = key_end - key0;  // rows [live, 128) of V_j are not keys
         if (side == 0 && live < kN) {
-          if (!(ok = wait(bVFull0 + (gx + j) % Ly::kVStages, (gx + j) / Ly::kVStages))) break;
+          if (!(ok = wait_w(bVFull0 + (gx + j) % Ly::kVStages, (gx + j) / Ly::kVStages))) break;
           uint8_t* vt = sgen + Ly::kV + ((gx + j) % Ly::kVStages) * Ly::kTile;
           const int chunks = (kN - live) * 128 / 16;
           for (int hf = 0; hf < Ly::kHalves; ++hf) {
@@ -742,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // swizzle) in its own 4 KB of shared memory; lane 0 writes the block
       // out with one asynchronous tensor store when all 32 rows are query
       // rows of this sequence, else the warp stores the live rows itself.
-      if (!(ok = wait(side ? bPvB : bPvA, ix))) break;
+      if (!(ok = wait_w(side ? bPvB : bPvA, ix))) break;
       tc_fence_after();
       uint32_t o[D];
       if constexpr (D == 128) {
@@ -933,18 +969,25 @@ int64_t total_slots_of(const AttnArgs& a) {
   return static_cast<int64_t>(a.hkv) * pairs * (a.num_seqs - a.num_decode) * max_level_of(a);
 }
 
+// Lets each instantiation use the layout's dynamic shared memory (once per
+// device and instantiation).
+template <typename K>
+cudaError_t allow_smem(K kernel, int bytes, bool (&done)[64]) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && done[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < 64) done[dev] = true;
+  return e;
+}
+
 template <int D, bool kFused>
 cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   using Ly = PpLayout<D>;
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, kFused>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  static bool done[2][64] = {};
+  auto kernel = a.wait_ns ? prefill_tc_kernel<D, kFused, false, true> : prefill_tc_kernel<D, kFused>;
+  cudaError_t e = allow_smem(kernel, Ly::kAlloc, done[a.wait_ns ? 1 : 0]);
+  if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mo, mkn, mvn, mq64;
   memset(&mkn, 0, sizeof(mkn));  // unused without the fused scatter
   memset(&mvn, 0, sizeof(mvn));
@@ -958,11 +1001,11 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   if (a.max_ctas > 0 && a.max_ctas < sms) sms = a.max_ctas;  // SMs left to a concurrent decode
   const int grid = total < sms ? total : sms;
   if (grid <= 0) return cudaSuccess;
-  cudaError_t e = a.sched_zeroed ? cudaSuccess : cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
+  e = a.sched_zeroed ? cudaSuccess : cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
   if (e != cudaSuccess) return e;
   count_launch();
   const int max_level = max_level_of(a);
-  e = launch_prio(prefill_tc_kernel<D, kFused>, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
+  e = launch_prio(kernel, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
                   a.has_priority, a.priority, mq, mk, mv, mo, mkn, mvn, mq64, a, total, max_level);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -975,15 +1018,10 @@ int64_t cascade_tc_slots(const AttnArgs& a) {
 template <int D>
 cudaError_t launch_casc_d(const AttnArgs& a, cudaStream_t st) {
   using Ly = PpLayout<D>;
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, false, true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  static bool done[2][64] = {};
+  auto kernel = a.wait_ns ? prefill_tc_kernel<D, false, true, true> : prefill_tc_kernel<D, false, true>;
+  cudaError_t e = allow_smem(kernel, Ly::kAlloc, done[a.wait_ns ? 1 : 0]);
+  if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mo, mkn, mvn, mq64;
   memset(&mkn, 0, sizeof(mkn));
   memset(&mvn, 0, sizeof(mvn));
@@ -995,10 +1033,10 @@ cudaError_t launch_casc_d(const AttnArgs& a, cudaStream_t st) {
   const int sms = device_num_sms();
   const int grid = total < sms ? total : sms;
   if (grid <= 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
+  e = cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
   if (e != cudaSuccess) return e;
   count_launch();
-  e = launch_prio(prefill_tc_kernel<D, false, true>, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
+  e = launch_prio(kernel, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
                   a.has_priority, a.priority, mq, mk, mv, mo, mkn, mvn, mq64, a, total, 1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -41,11 +41,30 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Non-blocking test of a phase (mbarrier.try_wait may instead suspend the
+// thread inside the hardware until the phase completes).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; give up after
-// `limit_ns` nanoseconds of wall time and return false.
+// `limit_ns` nanoseconds of wall time and return false.  Limits under 1 ms
+// poll without suspending, so that they hold however short they are (a
+// suspended try_wait can outlast them); longer ones suspend between tries.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  if (limit_ns < 1000000ull) {
+    while (!mbar_test_wait(bar, parity))
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+  }
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
@@ -82,6 +101,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
+}
+
+// Tensor prefetch global -> L2: no shared memory and no completion to wait
+// for; parts of the box outside the tensor are ignored.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
 }
 
 // Tensor store shared -> global (bulk-group completion).  The shared-memory

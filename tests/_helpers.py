@@ -148,3 +148,84 @@ def assert_close(got, expect, what=""):
     assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS, \
         f"{what}: max abs {d.max():.3g} mean abs {d.mean():.3g}"
     return float(d.max()), float(d.mean())
+
+
+class FullOracle:
+    """Every output row of a full-size step against the oracle.
+
+    The blocks the step's sequences read (their tables and the copy-on-write
+    sources) and the new-token rows are copied on the device BEFORE the step
+    runs.  ``check`` then evaluates the oracle over chunks of sequences, each
+    from a host fp64 copy of just the blocks it needs, and bounds max-abs and
+    mean-abs over all T x Hq x D outputs.
+    """
+
+    def __init__(self, lay, g, chunk_bytes=256 << 20):
+        self.lay = lay
+        ids = set()
+        for t in lay.tables:
+            ids.update(int(b) for b in t)
+        ids.update(int(a) for a, _ in lay.cow_pairs.tolist())
+        self.ids = sorted(ids)
+        self.pos = {b: i for i, b in enumerate(self.ids)}
+        idx = torch.tensor(self.ids, dtype=torch.long, device=g["k_cache"].device)
+        self.kc = g["k_cache"].index_select(0, idx)
+        self.vc = g["v_cache"].index_select(0, idx)
+        self.q, self.k, self.v = g["q"].clone(), g["k"].clone(), g["v"].clone()
+        per_block = lay.block_size * lay.num_kv_heads * lay.head_dim * 8
+        self.max_blocks = max(1, chunk_bytes // per_block)
+
+    def _chunks(self):
+        lay = self.lay
+        cur, nblk = [], 0
+        for s in range(lay.num_seqs):
+            n = len(lay.tables[s])
+            if cur and nblk + n > self.max_blocks:
+                yield cur
+                cur, nblk = [], 0
+            cur.append(s)
+            nblk += n
+        if cur:
+            yield cur
+
+    def check(self, out, what=""):
+        lay = self.lay
+        bs = lay.block_size
+        qsl = lay.query_start_loc
+        cow = {int(d): int(s) for s, d in lay.cow_pairs.tolist()}
+        worst, total, count = 0.0, 0.0, 0
+        for seqs in self._chunks():
+            blocks = sorted({int(b) for s in seqs for b in lay.tables[s]} |
+                            {cow[int(b)] for s in seqs for b in lay.tables[s] if int(b) in cow})
+            local = {b: i for i, b in enumerate(blocks)}
+            sel = torch.tensor([self.pos[b] for b in blocks], dtype=torch.long,
+                               device=self.kc.device)
+            kc = f64(self.kc.index_select(0, sel))
+            vc = f64(self.vc.index_select(0, sel))
+            pairs = [(local[cow[b]], local[b]) for b in blocks if b in cow]
+            if pairs:
+                kc, vc = ref.copy_blocks(kc, vc, np.array(pairs, dtype=np.int64))
+            rows = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in seqs]).astype(np.int64)
+            slots = lay.slot_mapping[rows].astype(np.int64)
+            lslots = np.array([local[int(x) // bs] * bs + int(x) % bs if x >= 0 else -1
+                               for x in slots], dtype=np.int64)
+            ti = torch.from_numpy(rows).to(self.q.device)
+            kc, vc = ref.write_kv(kc, vc, f64(self.k.index_select(0, ti)),
+                                  f64(self.v.index_select(0, ti)), lslots, bs)
+            qlens = [int(qsl[s + 1] - qsl[s]) for s in seqs]
+            tables = metadata.pad_block_tables([[local[int(b)] for b in lay.tables[s]]
+                                                for s in seqs])
+            expect = ref.attention(f64(self.q.index_select(0, ti)), kc, vc,
+                                   metadata.query_start_loc(qlens),
+                                   [int(lay.seq_lens[s]) for s in seqs], tables, bs, lay.scale,
+                                   lay.num_kv_heads)
+            got = f64(out.index_select(0, ti))
+            assert np.isfinite(got).all(), f"{what}: non-finite output"
+            d = np.abs(got - expect)
+            worst = max(worst, float(d.max()))
+            total += float(d.sum())
+            count += d.size
+        mean = total / max(count, 1)
+        assert count == lay.num_tokens * lay.num_q_heads * lay.head_dim
+        assert worst <= MAX_ABS and mean <= MEAN_ABS, f"{what}: max abs {worst:.3g} mean abs {mean:.3g}"
+        return worst, mean

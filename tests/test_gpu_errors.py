@@ -131,3 +131,41 @@ def test_unsupported_head_dim_is_refused():
     with pytest.raises(pa.PaError, match="UNSUPPORTED"):
         pa.attention(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"], md["bt"],
                      num_decode_seqs=0, max_query_len=2, max_seq_len=5)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two-calls", "fused-scatter"])
+def test_pipeline_wait_gives_up_then_next_call_is_exact(fused):
+    # The tensor-core prefill waits on shared-memory barriers for its copies
+    # and products.  A 1 ns limit makes its first waits run out on purpose:
+    # the kernel must set DEV_TIMEOUT, drain what it has in flight, free its
+    # tensor memory and return, leaving the context usable.  The next call,
+    # with the default limit, must then match the oracle.
+    lay = workloads.custom_layout("timeout", [0, 0, 40, 0], [700, 300, 129, 64], 8, 2, 128, 16,
+                                  400, 21)
+    ts = workloads.make_tensors(lay, seed=5, poison=True)            # CPU copies for the oracle
+    g = {k: v.to(DEV) for k, v in ts.items()}
+    md = H.device_meta(lay, DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def step():
+        kw = dict(num_decode_seqs=lay.num_decode_seqs, max_query_len=lay.max_query_len,
+                  max_seq_len=lay.max_seq_len, scale=lay.scale, err=err)
+        if fused:
+            return pa.write_kv_attention(g["q"], g["k"], g["v"], g["k_cache"], g["v_cache"],
+                                         md["slots"], md["qsl"], md["seq_lens"], md["bt"], **kw)
+        pa.write_kv(g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"], err=err)
+        return pa.attention(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"],
+                            md["bt"], **kw)
+
+    prev = pa.set_wait_limit_ns(1)
+    try:
+        step()
+        torch.cuda.synchronize()                     # the call returned; no CUDA error
+    finally:
+        pa.set_wait_limit_ns(prev)
+    assert int(err.item()) & pa.DEV_TIMEOUT
+    err.zero_()
+    out = step()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    H.assert_close(H.f64(out), H.oracle_full(lay, ts), "after a timed-out call")

@@ -115,10 +115,13 @@ def test_fused_decode_rows_on_prefill_kernel(lay):
 def test_fused_full_size(cfg):
     lay = workloads.config_layout(cfg, 0)
     outs, caches = [], []
+    full = None
     for fused in (False, True):
         g = workloads.make_tensors(lay, seed=3, device=DEV)
         md = H.device_meta(lay, DEV)
         err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        if fused and cfg in (2, 3, 4):
+            full = H.FullOracle(lay, g)        # every row of the fused step vs the oracle
         if fused:
             if len(lay.cow_pairs):
                 pa.copy_blocks(g["k_cache"], g["v_cache"], md["pairs"], err=err)
@@ -140,6 +143,8 @@ def test_fused_full_size(cfg):
         _close(outs[0], outs[1])
     assert torch.equal(_bits(caches[0][0]), _bits(caches[1][0]))
     assert torch.equal(_bits(caches[0][1]), _bits(caches[1][1]))
+    if full is not None:
+        full.check(outs[1], f"fused/{lay.name}")
 
 
 def test_fused_bad_slot_sets_flag():

@@ -6,9 +6,10 @@ memory is reserved up front, or a loop that must not call cudaMalloc because
 it can wait for the whole device.  pa_attention_noalloc takes no workspace;
 its split-KV scratch is a static device array inside the library.  These
 tests call it through the C ABI and check that it gives the same output as
-pa_attention with a caller-provided workspace, on two calls in a row (the
-second call finds the first call's partial results still in the array), and
-that it refuses a batch that needs more scratch than the array holds.
+pa_attention with a caller-provided workspace and agrees with the fp64
+oracle, on two calls in a row (the second call finds the first call's
+partial results still in the array), and that it refuses a batch that needs
+more scratch than the array holds.
 
 This file is collected last on purpose: it only adds an entry point and must
 pass both alone in a fresh process and after every other test.
@@ -45,23 +46,37 @@ def test_noalloc_matches_attention_on_two_calls_in_a_row():
     for i, lay in enumerate(_layouts()):
         need = pa.workspace_size(lay.num_decode_seqs, lay.num_q_heads, lay.num_kv_heads,
                                  lay.head_dim, lay.max_seq_len)
-        assert 0 < need <= pa.NOALLOC_SCRATCH_BYTES
-        g = workloads.make_tensors(lay, seed=40 + i, device=DEV, poison=True)
+        # more than the header alone: the decode rows need split-KV partials
+        header = pa.workspace_size(0, lay.num_q_heads, lay.num_kv_heads, lay.head_dim,
+                                   lay.max_seq_len)
+        assert header < need <= pa.NOALLOC_SCRATCH_BYTES
+        ts = workloads.make_tensors(lay, seed=40 + i, poison=True)    # CPU copies for the oracle
+        g = {k: v.to(DEV) for k, v in ts.items()}
         md = H.device_meta(lay, DEV)
         pa.write_kv(g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"])
         expect = pa.attention(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"],
                               md["bt"], num_decode_seqs=lay.num_decode_seqs,
                               max_query_len=lay.max_query_len, max_seq_len=lay.max_seq_len,
                               scale=lay.scale)
-        out = torch.empty_like(g["q"])
-        err = torch.zeros(1, dtype=torch.int32, device=DEV)
-        pa.attention_noalloc(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"],
-                             md["bt"], out=out, num_decode_seqs=lay.num_decode_seqs,
-                             max_query_len=lay.max_query_len, max_seq_len=lay.max_seq_len,
-                             scale=lay.scale, err=err)
         torch.cuda.synchronize()
-        assert int(err.item()) == 0
-        H.assert_close(H.f64(out), H.f64(expect), lay.name)
+        oracle = H.oracle_full(lay, ts)
+        for call in range(2):
+            out = torch.empty_like(g["q"])
+            err = torch.zeros(1, dtype=torch.int32, device=DEV)
+            before = pa.kernel_launches()
+            pa.attention_noalloc(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"],
+                                 md["bt"], out=out, num_decode_seqs=lay.num_decode_seqs,
+                                 max_query_len=lay.max_query_len, max_seq_len=lay.max_seq_len,
+                                 scale=lay.scale, err=err)
+            torch.cuda.synchronize()
+            launched = pa.kernel_launches() - before
+            assert int(err.item()) == 0
+            # decode and the split combine (plus the prefill kernel for prefill rows):
+            # the partials really go through the static array
+            has_prefill = lay.num_seqs > lay.num_decode_seqs
+            assert launched == 2 + int(has_prefill), launched
+            H.assert_close(H.f64(out), H.f64(expect), f"{lay.name} call {call}")
+            H.assert_close(H.f64(out), oracle, f"{lay.name} call {call} vs oracle")
 
 
 def test_noalloc_refuses_batches_beyond_its_scratch():
