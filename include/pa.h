@@ -160,9 +160,9 @@ int pa_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_strid
  * groups those new keys into 128-key tiles starting at c_s (the cached
  * history keeps its tiles from position 0), so the result is bit-identical
  * to the two calls for sequences without history and otherwise equal up to
- * the order of the fp32 sums.  Any other step (decode rows present, block
- * size below 8, or scale <= 0) scatters first and then attends, bit-identical
- * to the two calls.
+ * the order of the fp32 sums.  Any other step (decode rows present, or
+ * scale <= 0) scatters first and then attends, bit-identical to the two
+ * calls.
  * Errors: as pa_write_kv and pa_attention.
  */
 int pa_write_kv_attention(void* out, int64_t out_stride_t, const void* q, int64_t q_stride_t,

@@ -26,22 +26,31 @@
 // head, keys are a chunk of the shared prefix with no causal mask, and the
 // epilogue writes fp32 partials (O, m, l) for the split combine.
 //
-// Warp roles (384 threads, three warpgroups):
-//   warps 0-3   softmax + epilogue of tile A (thread r = query row r = TMEM lane r)
-//   warps 4-7   softmax + epilogue of tile B
+// Warp roles (512 threads, four warpgroups):
+//   warps 0-3   softmax of tile A (thread r = query row r = TMEM lane r)
+//   warps 4-7   softmax of tile B
 //   warp 8      TMA producer of K_j (2-stage ring)
 //   warp 9      TMEM allocation and MMA issue (one lane)
 //   warp 10     TMA producer of V_j (2-stage ring)
 //   warp 11     scheduler: draws items from the global queue, hands them to the
 //               other roles through a 2-entry shared-memory ring, and loads
 //               each item's Q_A/Q_B once the previous item's last S is done
+//   warps 12-15 epilogue: when a side has reported an item's last P, it hands
+//               each row's sum l and reference maximum m to these warps
+//               through a shared-memory slot and goes straight on to the next
+//               item; they wait for the side's last product, read O out of
+//               TMEM, release it to the next item's products, normalise,
+//               pack and store each row
 // The producers' lanes resolve a tile's blocks through the block table and
-// issue one TMA box each.
-// The softmax warpgroups raise their register limit to 200 and the third
-// warpgroup lowers its to 104 (256*200 + 128*104 = 64512 = 384*168 launched;
-// per SM sub-partition 200+200+104 registers x 32 lanes <= 16384), so a
-// softmax thread holds its whole 128-score row after one TMEM load and the
-// producer, MMA and scheduler code runs without spills.
+// issue one TMA box each (blocks of fewer than 8 rows: 16-byte cp.async).
+// Registers (setmaxnreg, each warpgroup at the top of its own branch): the
+// softmax warpgroups 200 each, the producer/MMA/scheduler warpgroup 64 and
+// the epilogue warpgroup 48, which adds up to the 4 x 128 a thread is
+// launched with (per SM sub-partition 200+200+64+48 registers x 32 lanes =
+// 16384).  A launch of 512 threads compiles every single instruction within
+// 128 registers, so a softmax row of 128 scores is read from TMEM as two
+// 64-column loads; the MMA lane keeps each shared-memory descriptor as one
+// 32-bit word to fit in its 64.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // P (bf16, two per 32-bit column) is written over the first 64 columns of its
 // own S and read from there as the A operand of O += P V.  Per key tile j the
@@ -88,7 +97,14 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kVWarp = 10;
 constexpr int kSchedWarp = 11;
-constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 12;  // warps 12-15: epilogue
+constexpr int kThreads = 512;
+// setmaxnreg split of the 128 registers a thread is launched with
+constexpr int kSoftmaxRegs = 200;
+constexpr int kProducerRegs = 64;
+constexpr int kEpiRegs = 48;
+static_assert(2 * kSoftmaxRegs + kProducerRegs + kEpiRegs == 4 * 65536 / kThreads,
+              "the warpgroups' register limits must add up to the launch's");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -109,6 +125,11 @@ __device__ __forceinline__ float2 f2_split(uint64_t v) {
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
@@ -132,10 +153,11 @@ struct PpLayout {
   static constexpr int kQ = 0;  // Q of side A, then of side B
   static constexpr int kK = 2 * kTile;
   static constexpr int kV = kK + kKStages * kTile;
-  static constexpr int kStage = kV + kVStages * kTile;  // output staging, 4 KB per softmax warp
-  static constexpr int kBar = kStage + kSoftmaxWarps * 4096;
+  static constexpr int kEpi = kV + kVStages * kTile;  // softmax -> epilogue hand-off slots
+  static constexpr int kBar = kEpi + 5 * 1024;
   static constexpr int kBytes = kBar + 512;  // barriers, TMEM slot, flags, item ring
   static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1 KB
+  static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
   __host__ __device__ static constexpr int q(int side) { return kQ + side * kTile; }
 };
 
@@ -144,7 +166,7 @@ enum : int {
   bKFull0, bKFull1, bKEmpty0, bKEmpty1,
   bVFull0, bVFull1, bVEmpty0, bVEmpty1,
   bSA, bSB, bPA, bPB, bPvA, bPvB, bOFreeA, bOFreeB, bDrain,
-  bItemFull0, bItemFull1, bItemEmpty0, bItemEmpty1, kNumBars
+  bItemFull0, bItemFull1, bItemEmpty0, bItemEmpty1, bLA0, bLA1, bLB0, bLB1, kNumBars
 };
 
 
@@ -159,6 +181,17 @@ struct Item {
   int pk;  // packed: a tile of <= 64 query tokens holds two heads (rows 0-63: head
            // h, rows 64-127: head h + 1), so the item covers four heads
 };
+
+// What a softmax side hands to the epilogue warps when it has reported an
+// item's last P: each row's sum l and reference maximum m (log2 domain), and
+// the item (n = 0 in side A's slot: no more items).  Two slots per side, by
+// the side's item parity.
+struct EpiSlot {
+  float l[kM];
+  float m[kM];
+  Item it;
+};
+static_assert(4 * sizeof(EpiSlot) <= 5 * 1024, "hand-off slots");
 
 // Key range [key0, key_end) of tile j of an item.  Without the fused scatter
 // the tiles are 128-position windows from position 0.  With it, the cached
@@ -296,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_slot = bar0 + 8 * kNumBars;
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(sgen + Ly::kBar + 8 * kNumBars + 4);
+  // items side A has handed to the epilogue warps when it runs out of items
+  volatile int* epi_total = reinterpret_cast<volatile int*>(sgen + Ly::kBar + 8 * kNumBars + 8);
   Item* ring = reinterpret_cast<Item*>(sgen + Ly::kBar + kRingOffset);
 #define BAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
 
@@ -305,11 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      const bool many = i == bPA || i == bPB || i == bOFreeA || i == bOFreeB;
+      const bool many = i == bPA || i == bPB || i == bOFreeA || i == bOFreeB || i == bLA0 ||
+                        i == bLA1 || i == bLB0 || i == bLB1;
       const bool readers = i == bItemEmpty0 || i == bItemEmpty1;
       mbar_init(BAR(i), many ? 128u : (readers ? kItemReaders : 1u));
     }
     *abort_flag = 0u;
+    *epi_total = INT_MAX;
     fence_barrier_init();
   }
   if (threadIdx.x == 32 * kProducerWarp) {
@@ -389,7 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  if (warp >= kProducerWarp) regs_decrease<104>();
+  EpiSlot* epi = reinterpret_cast<EpiSlot*>(sgen + Ly::kEpi);  // [parity][side]
+  // Each warpgroup's register limit is set at the top of its own branch, so
+  // that the compiler allocates each role's code within its own limit.
+  if (warp >= kProducerWarp && warp < kEpiWarp0) {
+  regs_decrease<kProducerRegs>();
   if (warp == kSchedWarp) {
     // ------------------------------------------------------------ scheduler
     if (lane == 0) {
@@ -444,8 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (q_issued > 0) mbar_wait(BAR(bQFull), (q_issued - 1) & 1, kWaitNs);
     }
     __syncwarp();
-  }
-  if (warp == kProducerWarp || warp == kVWarp) {
+  } else if (warp == kProducerWarp || warp == kVWarp) {
     // ------------------------------------------------------------ producers
     // warp 8: the K tiles; warp 10: the V tiles.  Cached positions come from
     // the paged cache, one TMA box per block (lane b issues box b).  With the
@@ -470,19 +510,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // while this warp would otherwise wait for a free stage, and at the
     // latest before that tile's stage is refilled.
     int pend_g = -1;
-    Item pend_I{};
+    int pend_row0 = 0, pend_rows = 0, pend_hk = 0;  // first input row, row count, kv head
     auto scatter = [&]() -> bool {
       const int g = pend_g;
       if (!wait_w(full0 + g % nst, g / nst)) return false;
       const uint8_t* sg = sgen + (stage0 - base) + (g % nst) * Ly::kTile;
-      const Item& P = pend_I;
-      const int rows = min(kM, P.qn - P.i0);
       const int64_t nslots = static_cast<int64_t>(a.num_blocks) << a.bs_log2;
       __nv_bfloat16* cw = static_cast<__nv_bfloat16*>(const_cast<void*>(is_k ? a.k_cache : a.v_cache)) +
-                          static_cast<int64_t>(P.hk) * D;
+                          static_cast<int64_t>(pend_hk) * D;
 #pragma unroll 1
-      for (int r = lane; r < rows; r += 32) {
-        const int sl = __ldg(a.slots + P.t0 + P.i0 + r);
+      for (int r = lane; r < pend_rows; r += 32) {
+        const int sl = __ldg(a.slots + pend_row0 + r);
         if (sl >= nslots) {
           flag_error(a.err, PA_DEV_BAD_SLOT);
         } else if (sl >= 0) {
@@ -541,6 +579,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           last = gt;
           continue;
         }
+        if (bs < 8) {
+          // Blocks of fewer than 8 rows: a box would not fill whole 8-row
+          // swizzle atoms, so the lanes gather the rows themselves with
+          // 16-byte cp.async into the same 128-byte-swizzled layout (lane l
+          // takes rows l, l + 32, ...), wait for their own copies and make
+          // them visible to the tensor core (proxy fence) before lane 0
+          // reports the stage full.  Rows past the tile's last key are left
+          // as they are, as with boxes.
+          if (!(ok = before_refill(st))) break;
+          if (gt >= nst && !(ok = wait_w(empty0 + st, gt / nst - 1))) break;
+          const char* cbase = static_cast<const char*>(is_k ? a.k_cache : a.v_cache);
+#pragma unroll 1
+          for (int rr = lane; rr < key_end - key0; rr += 32) {
+            const int pos = key0 + rr;
+            const int pb = __ldg(bt + (pos >> a.bs_log2));
+            if (pb < 0 || pb >= a.num_blocks) {
+              flag_error(a.err, PA_DEV_BAD_BLOCK);
+              continue;
+            }
+            const int64_t sl = (static_cast<int64_t>(pb) << a.bs_log2) + (pos & (bs - 1));
+            const char* src = cbase + (sl * a.hkv + I.hk) * (D * 2);
+            const uint32_t drow = stile + rr * 128;
+#pragma unroll
+            for (int c = 0; c < kCpr; ++c)
+              cp_async16(drow + (c >> 3) * Ly::kHalf + (((c & 7) ^ (rr & 7)) << 4), src + c * 16,
+                         true);
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(full0 + st));
+          last = gt;
+          continue;
+        }
         // cached positions: one box per block
         const int nbox = (key_end - key0 + R - 1) / R;
         int slot = -1;
@@ -571,7 +644,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 0 .. rows - 1: store them into their slots once it has landed.
         if (pend_g >= 0 && !(ok = scatter())) break;
         pend_g = gt - 1;
-        pend_I = I;
+        pend_row0 = I.t0 + I.i0;
+        pend_rows = min(kM, I.qn - I.i0);
+        pend_hk = I.hk;
       }
     }
     if (ok && pend_g >= 0) ok = scatter();
@@ -581,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(BAR(full0 + t % nst), (t / nst) & 1, kWaitNs);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_bf16(kM, kN, false);
     constexpr uint32_t kIdO = idesc_bf16(kM, D, true);
@@ -593,24 +668,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dQ0 = smem_desc_sw128(base + Ly::kQ, 16, 1024);
     const uint64_t dK0 = smem_desc_sw128(base + Ly::kK, 16, 1024);
     const uint64_t dV0 = smem_desc_sw128(base + Ly::kV, Ly::kHalf, 1024);
+    const uint32_t dHi = static_cast<uint32_t>(dQ0 >> 32);  // the same for all three
     const uint32_t tS0 = tmem, tO0 = tmem + 256;
     // S of one side for key tile g
     auto issue_s = [&](int side, int g) {
-      const uint64_t a0 = dQ0 + static_cast<uint64_t>(Ly::q(side) >> 4);
-      const uint64_t b0 = dK0 + static_cast<uint64_t>((g % Ly::kKStages) * (Ly::kTile >> 4));
+      const uint32_t a0 = opaque_u32(static_cast<uint32_t>(dQ0) + (Ly::q(side) >> 4));
+      const uint32_t b0 = opaque_u32(static_cast<uint32_t>(dK0) +
+                                     (g % Ly::kKStages) * (Ly::kTile >> 4));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * Ly::kHalf + (kk & 3) * 32) >> 4);
-        mma_f16_ss(tS0 + side * 128, a0 + off, b0 + off, kIdS, kk > 0 ? 1u : 0u);
+        const uint32_t off = ((kk >> 2) * Ly::kHalf + (kk & 3) * 32) >> 4;
+        mma_f16_ss_lo(tS0 + side * 128, a0 + off, b0 + off, dHi, kIdS, kk > 0 ? 1u : 0u);
       }
       mma_commit(BAR(side ? bSB : bSA));
     };
     auto issue_pv = [&](int side, int g, bool acc) {
-      const uint64_t v0 = dV0 + static_cast<uint64_t>((g % Ly::kVStages) * (Ly::kTile >> 4));
+      const uint32_t v0 = opaque_u32(static_cast<uint32_t>(dV0) +
+                                     (g % Ly::kVStages) * (Ly::kTile >> 4));
 #pragma unroll
       for (int kk = 0; kk < kN / 16; ++kk)
-        mma_f16_ts(tO0 + side * 128, tS0 + side * 128 + kk * 8, v0 + static_cast<uint64_t>(kk * (2048 >> 4)),
-                   kIdO, (acc || kk > 0) ? 1u : 0u);
+        mma_f16_ts_lo(tO0 + side * 128, tS0 + side * 128 + kk * 8, v0 + kk * (2048 >> 4), dHi,
+                      kIdO, (acc || kk > 0) ? 1u : 0u);
     };
     // One lane issues everything; the V rows past the last key of a partial
     // tile are zeroed by softmax A before it reports its P.  This lane needs
@@ -673,9 +751,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(BAR(bDrain), 0, kWaitNs);
     }
     __syncwarp();
+  }
   } else if (warp < kProducerWarp) {
     // ------------------------------------------------------------ softmax A / B
-    regs_increase<200>();
+    regs_increase<kSoftmaxRegs>();
     const int side = warp >> 2;  // 0: A (warps 0-3), 1: B (warps 4-7)
     const int r = threadIdx.x - side * 128;  // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -686,7 +765,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       Item I;
-      if (!next_item(k, I, true)) break;
+      if (!next_item(k, I, true)) {
+        if (side == 0 && r == 0) *epi_total = ix;  // no more items: the epilogue stops after ix - 1
+        break;
+      }
       if (side == 1 && I.h[1] < 0) continue;
       const int i = I.i0 + (I.pk ? (r & (kM / 2 - 1)) : r);  // this row's query token
       const int lim = kCasc ? I.kv_end - 1 : I.c + i;  // last key position this row sees
@@ -700,11 +782,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_keys(I, j, kFused, key0, key_end, kCasc);
         const bool full = key0 + kN - 1 <= lim && key0 + kN <= key_end;
         uint32_t sr[128];
-        tmem_ld128(tS, sr);
+        tmem_ld64(tS, *reinterpret_cast<uint32_t(*)[64]>(sr));
+        tmem_ld64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(sr + 64));
         tmem_wait_ld();
         // Row maximum of the raw scores (scale > 0, so it commutes with the
         // scaling); masked keys become -inf.
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // max over the 8-column block starting at column e8
+        auto block_max = [&](int e8) {
+          const int q = (e8 >> 3) & 3;
+          mx[q] = max3(mx[q], __uint_as_float(sr[e8]), __uint_as_float(sr[e8 + 1]));
+          mx[q] = max3(mx[q], __uint_as_float(sr[e8 + 2]), __uint_as_float(sr[e8 + 3]));
+          mx[q] = max3(mx[q], __uint_as_float(sr[e8 + 4]), __uint_as_float(sr[e8 + 5]));
+          mx[q] = max3(mx[q], __uint_as_float(sr[e8 + 6]), __uint_as_float(sr[e8 + 7]));
+        };
         if (!full) {
           const int last = min(lim, key_end - 1) - key0;  // last visible column of this row
 #pragma unroll
@@ -712,32 +803,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (e2 > last) sr[e2] = __float_as_uint(-INFINITY);
         }
 #pragma unroll
-        for (int e2 = 0; e2 < 128; e2 += 8) {
-          const int q = (e2 >> 3) & 3;
-          mx[q] = max3(mx[q], __uint_as_float(sr[e2]), __uint_as_float(sr[e2 + 1]));
-          mx[q] = max3(mx[q], __uint_as_float(sr[e2 + 2]), __uint_as_float(sr[e2 + 3]));
-          mx[q] = max3(mx[q], __uint_as_float(sr[e2 + 4]), __uint_as_float(sr[e2 + 5]));
-          mx[q] = max3(mx[q], __uint_as_float(sr[e2 + 6]), __uint_as_float(sr[e2 + 7]));
-        }
+        for (int e8 = 0; e8 < 128; e8 += 8) block_max(e8);
         const float mt = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]) * a.scale_log2;
         const float m_new = mt > m_used + 8.f ? mt : m_used;
         const float ref = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - ref);
-        // P = 2^(s * scale - m), rounded to bf16 and packed in pairs into sr[0..1]
+        // P = 2^(s * scale - m), rounded to bf16 and packed in pairs into sr[0..63]
         const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
         const uint64_t nref2 = f2(-ref, -ref);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // four (+0, +0) pair sums
         uint32_t* flat = sr;
+        auto block_exp = [&](int e8) {
 #pragma unroll
-        for (int e2 = 0; e2 < 128; e2 += 2) {
-          const uint64_t x = f2_fma(f2(__uint_as_float(flat[e2]), __uint_as_float(flat[e2 + 1])),
-                                    sc2, nref2);
-          const float2 xc = f2_split(x);
-          const uint64_t pp = f2(ex2(xc.x), ex2(xc.y));
-          acc[(e2 >> 1) & 3] = f2_add(acc[(e2 >> 1) & 3], pp);
-          const float2 pc = f2_split(pp);
-          flat[e2 >> 1] = pack_bf16(pc.x, pc.y);
-        }
+          for (int e2 = e8; e2 < e8 + 8; e2 += 2) {
+            const uint64_t x = f2_fma(f2(__uint_as_float(flat[e2]), __uint_as_float(flat[e2 + 1])),
+                                      sc2, nref2);
+            const float2 xc = f2_split(x);
+            const uint64_t pp = f2(ex2(xc.x), ex2(xc.y));
+            acc[(e2 >> 1) & 3] = f2_add(acc[(e2 >> 1) & 3], pp);
+            const float2 pc = f2_split(pp);
+            flat[e2 >> 1] = pack_bf16(pc.x, pc.y);
+          }
+        };
+#pragma unroll
+        for (int e8 = 0; e8 < 128; e8 += 8) block_exp(e8);
         const float2 s01 = f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
         l = l * alpha + (s01.x + s01.y);
         tmem_st64(tS, *reinterpret_cast<uint32_t(*)[64]>(sr));
@@ -771,94 +860,133 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(BAR(side ? bPB : bPA));
       }
       if (!ok) break;
-      // epilogue: wait for this side's last product and read O out of TMEM;
-      // release O to the next item's products at once, then normalise, pack
-      // and store from registers.  Each warp stages 64 columns of its 32 rows
-      // (128 B per row, 16-byte pieces XOR-swizzled by row: the TMA 128-byte
-      // swizzle) in its own 4 KB of shared memory; lane 0 writes the block
-      // out with one asynchronous tensor store when all 32 rows are query
-      // rows of this sequence, else the warp stores the live rows itself.
-      if (!(ok = wait_w(side ? bPvB : bPvA, ix))) break;
-      tc_fence_after();
-      uint32_t o[D];
-      if constexpr (D == 128) {
-        tmem_ld128(tO, o);
-      } else {
-        tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(o));
-        tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(BAR(side ? bOFreeB : bOFreeA));
-      if constexpr (kCasc) {
-        // this query row's partial over the chunk: unnormalised O, its
-        // reference m (log2 domain) and sum l, in the chunk's slot
-        const int row = I.h[side] * kM + r;
-        if (row < I.qn) {
-          const int seq = row / a.group;
-          const int head = I.hk * a.group + (row - seq * a.group);
-          const int64_t wr = (static_cast<int64_t>(I.t0) * a.num_decode + seq) * a.hq + head;
-          float4* dst = reinterpret_cast<float4*>(a.ws_o + wr * D);
-#pragma unroll
-          for (int c4 = 0; c4 < D / 4; ++c4)
-            dst[c4] = make_float4(__uint_as_float(o[4 * c4]), __uint_as_float(o[4 * c4 + 1]),
-                                  __uint_as_float(o[4 * c4 + 2]), __uint_as_float(o[4 * c4 + 3]));
-          a.ws_ml[wr * 2] = m_used;
-          a.ws_ml[wr * 2 + 1] = l;
-        }
-        gx += I.n;
-        ++ix;
-        continue;
-      }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-      for (int e2 = 0; e2 < D / 2; ++e2)
-        o[e2] = pack_bf16(__uint_as_float(o[2 * e2]) * inv, __uint_as_float(o[2 * e2 + 1]) * inv);
-      uint8_t* stg = sgen + Ly::kStage + warp * 4096;
-      const uint32_t stg_s = base + Ly::kStage + warp * 4096;
-      // query token of this warp's lane 0, and its head (packed: warps 0-1
-      // hold the first head's 64 tokens, warps 2-3 the second's)
-      const int wrow0 = I.i0 + (I.pk ? (warp & 1) * 32 : (warp & 3) * 32);
-      const int whead = I.h[side] + (I.pk ? ((warp & 3) >> 1) : 0);
-      const bool whole = wrow0 + 32 <= I.qn;
-      __nv_bfloat16* ohead = static_cast<__nv_bfloat16*>(a.out) +
-                             static_cast<int64_t>(whead) * D;
-#pragma unroll
-      for (int hh = 0; hh < D / 64; ++hh) {
-        if (lane == 0) bulk_wait_read();  // the previous store has read the staging buffer
-        __syncwarp();
-#pragma unroll
-        for (int piece = 0; piece < 8; ++piece)
-          *reinterpret_cast<uint4*>(stg + lane * 128 + ((piece ^ (lane & 7)) << 4)) =
-              make_uint4(o[hh * 32 + piece * 4], o[hh * 32 + piece * 4 + 1],
-                         o[hh * 32 + piece * 4 + 2], o[hh * 32 + piece * 4 + 3]);
-        if (whole) {
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tm_o, stg_s, whead * D + hh * 64, I.t0 + wrow0);
-            bulk_commit();
-          }
-        } else {
-          __syncwarp();
-#pragma unroll
-          for (int i4 = 0; i4 < 8; ++i4) {
-            const int rr = i4 * 4 + (lane >> 3);  // row within the warp's 32
-            const int piece = lane & 7;
-            const uint4 w =
-                *reinterpret_cast<const uint4*>(stg + rr * 128 + ((piece ^ (rr & 7)) << 4));
-            const int qi = wrow0 + rr;
-            if (qi < I.qn)
-              *reinterpret_cast<uint4*>(ohead + static_cast<int64_t>(I.t0 + qi) * a.out_stride +
-                                        hh * 64 + piece * 8) = w;
-          }
-          __syncwarp();
-        }
-      }
+      // Hand the row's sum and reference maximum to the epilogue warps, which
+      // wait for this side's last product, normalise O and store it, while
+      // this warp goes on to the next item.
+      EpiSlot& es = epi[(ix & 1) * 2 + side];
+      es.l[r] = l;
+      es.m[r] = m_used;
+      if (r == 0) es.it = I;
+      // Hand-off barriers alternate by item parity: a side cannot finish item
+      // k + 2 before the epilogue has released item k's O, so neither barrier
+      // runs more than one phase ahead of the epilogue's wait on it.
+      mbar_arrive(BAR((side ? bLB0 : bLA0) + (ix & 1)));
       gx += I.n;
       ++ix;
     }
-    if (lane == 0) bulk_wait();  // every tensor store of this warp is complete
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Warp 12 + q reads TMEM lanes 32q .. 32q + 31 (its query rows) of O.
+    // Per item: side A, then side B if the item has one.  O is read 16
+    // columns at a time; after the last chunk O is released to the next
+    // item's products.  Each thread normalises its row by 1 / l, packs it to
+    // bf16 and stores it straight to the output, 16 bytes at a time (these
+    // warps are off the softmax's critical path, so they need no staging
+    // buffer).  The shared-prefix mode writes fp32 partials (O, m, l).
+    regs_decrease<kEpiRegs>();
+    const int q4 = warp - kEpiWarp0;
+    const int r = q4 * 32 + lane;  // query row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    auto finish = [&](int side, int idx, int t0, int i0, int qn, int head, int pk, int hk) -> bool {
+      if (!wait_w(side ? bPvB : bPvA, idx)) return false;
+      tc_fence_after();
+      const EpiSlot& es = epi[(idx & 1) * 2 + side];
+      const float l = es.l[r];
+      const uint32_t tO = tmem + 256 + side * 128 + lane_off;
+      if constexpr (kCasc) {
+        // this query row's partial over the chunk: unnormalised O, its
+        // reference m (log2 domain) and sum l, in the chunk's slot (t0)
+        const int row = head * kM + r;
+        const bool live = row < qn;
+        float* dst = nullptr;
+        if (live) {
+          const int seq = row / a.group;
+          const int64_t wr = (static_cast<int64_t>(t0) * a.num_decode + seq) * a.hq + hk * a.group +
+                             (row - seq * a.group);
+          dst = a.ws_o + wr * D;
+          a.ws_ml[wr * 2] = es.m[r];
+          a.ws_ml[wr * 2 + 1] = l;
+        }
+#pragma unroll 1
+        for (int cc = 0; cc < D / 16; ++cc) {
+          uint32_t o[16];
+          tmem_ld16(tO + cc * 16, o);
+          tmem_wait_ld();
+          if (cc == D / 16 - 1) {
+            tc_fence_before();
+            mbar_arrive(BAR(side ? bOFreeB : bOFreeA));
+          }
+          if (live) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+              reinterpret_cast<float4*>(dst + cc * 16)[c4] =
+                  make_float4(__uint_as_float(o[4 * c4]), __uint_as_float(o[4 * c4 + 1]),
+                              __uint_as_float(o[4 * c4 + 2]), __uint_as_float(o[4 * c4 + 3]));
+          }
+        }
+        return true;
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const uint64_t inv2 = f2(inv, inv);
+      // this row's query token and head (packed: rows 64-127 are the next head)
+      const int i = i0 + (pk ? (r & (kM / 2 - 1)) : r);
+      const bool live = i < qn;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                            static_cast<int64_t>(t0 + (live ? i : 0)) * a.out_stride +
+                            static_cast<int64_t>(head + (pk ? (r >> 6) : 0)) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 16; ++cc) {  // 16-column chunks
+        uint32_t o[16];
+        tmem_ld16(tO + cc * 16, o);
+        tmem_wait_ld();
+        if (cc == D / 16 - 1) {
+          tc_fence_before();
+          mbar_arrive(BAR(side ? bOFreeB : bOFreeA));
+        }
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 on =
+              f2_split(f2_mul(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2));
+          w[e] = pack_bf16(on.x, on.y);
+        }
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 16);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+      return true;
+    };
+    // Wait for side A's hand-off of item ie (1), or learn that side A has no
+    // more items (0); -1: the wait ran out or the CTA gave up.  The stop word
+    // is looked at between suspending tries, and the warp takes the outcome
+    // together.
+    auto next_handoff = [&](int ie) -> bool {
+      const uint32_t bar = BAR(bLA0 + (ie & 1));
+      const uint32_t par = static_cast<uint32_t>(ie >> 1) & 1u;
+      const uint64_t limit = a.wait_ns ? a.wait_ns : kWaitNs;
+      const uint64_t t0 = globaltimer_ns();
+      int res;
+      while (true) {
+        if (kPoll ? mbar_test_wait(bar, par) : mbar_try_wait(bar, par)) { res = 1; break; }
+        if (*epi_total <= ie || *abort_flag) { res = 0; break; }
+        if (globaltimer_ns() - t0 > limit) { give_up(); res = 0; break; }
+      }
+      return __all_sync(0xffffffffu, res == 1);
+    };
+    int ie = 0, ieB = 0;
+    for (;;) {
+      if (!next_handoff(ie)) break;
+      const Item& I = epi[(ie & 1) * 2].it;
+      const int t0 = I.t0, i0 = I.i0, qn = I.qn, hA = I.h[0], hB = I.h[1], pk = I.pk, hk = I.hk;
+      if (!finish(0, ie, t0, i0, qn, hA, pk, hk)) break;
+      if (hB >= 0) {
+        if (!wait_w(bLB0 + (ieB & 1), ieB >> 1) || !finish(1, ieB, t0, i0, qn, hB, pk, hk)) break;
+        ++ieB;
+      }
+      ++ie;
+    }
   }
 #undef BAR
   tc_fence_before();
@@ -1062,7 +1190,6 @@ bool prefill_tc_supported(const AttnArgs& a) {
   if (env && strcmp(env, "mma") == 0) return false;
   if (a.head_dim != 64 && a.head_dim != 128) return false;
   if (!(a.scale_log2 > 0.f)) return false;  // the row maximum is taken before scaling
-  if (a.bs_log2 < 3) return false;  // TMA boxes of >= 8 rows keep 1 KB swizzle alignment
   if ((a.q_stride * 2) % 16 != 0 || (a.out_stride * 2) % 16 != 0) return false;
   if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k_cache) |
        reinterpret_cast<uintptr_t>(a.v_cache) | reinterpret_cast<uintptr_t>(a.out)) & 15u)
