@@ -173,7 +173,9 @@ enum : int {
 // Arrivals that release each item's ring entry: one lane of the K producer,
 // the MMA and the V producer warps, and every softmax thread.
 constexpr uint32_t kItemReaders = 3 + 32 * kSoftmaxWarps;
-constexpr int kRingOffset = 8 * 32;  // bytes after the barriers (TMEM slot + flags first)
+// The barrier area: the mbarriers, then the TMEM address, the abort flag and
+// the epilogue's stop word (4 bytes each), then the 2-entry item ring.
+constexpr int kRingOffset = (8 * kNumBars + 12 + 15) / 16 * 16;
 
 struct Item {
   int s, hk, h[2], t0, qn, c, i0, kv_end, n;  // h[1] < 0: no second tile
@@ -181,6 +183,9 @@ struct Item {
   int pk;  // packed: a tile of <= 64 query tokens holds two heads (rows 0-63: head
            // h, rows 64-127: head h + 1), so the item covers four heads
 };
+
+static_assert(kRingOffset + 2 * static_cast<int>(sizeof(Item)) <= 512,
+              "barriers, flags and item ring must fit the 512-byte barrier area");
 
 // What a softmax side hands to the epilogue warps when it has reported an
 // item's last P: each row's sum l and reference maximum m (log2 domain), and
