@@ -12,11 +12,14 @@
 // the same kv head (so every K/V tile feeds both), or one head when the group
 // has an odd head left over.  An item's cost is its number of 128-key tiles;
 // token tile t of a sequence with c cached tokens has cost ceil(c/128) + t + 1
-// (one less for a short last tile).  Slots enumerate items by that level,
+// (one less for a short last tile).  Items are listed by that level,
 // highest first, so the list is sorted by cost.  The grid is persistent (one
-// CTA per SM); a scheduler warp in each CTA takes the next slot from a global
-// counter (atomicAdd) whenever its CTA has room, so CTAs that drew cheap
-// items draw more and all finish together.
+// CTA per SM): CTA b starts with item b, and then a scheduler warp in each
+// CTA takes the next item number from a global counter (atomicAdd) whenever
+// its CTA has room, so CTAs that drew cheap items draw more and all finish
+// together.  The numbers cover existing items only (each CTA tabulates the
+// items per level in shared memory and maps a number to its item), so no draw
+// comes back empty.
 //
 // A token tile of at most 64 tokens (the tail of a chunk) is "packed" when
 // the group splits into fours: each side's 128 rows hold two heads (rows
@@ -143,6 +146,10 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+// The scheduler's table of items per cost level (ints, in shared memory);
+// with more levels it scans the slots instead.
+constexpr int kMaxLevels = 2048;
+
 template <int D>
 struct PpLayout {
   static constexpr int kHalves = D / 64;        // 64-element (128-byte) column chunks
@@ -155,7 +162,8 @@ struct PpLayout {
   static constexpr int kV = kK + kKStages * kTile;
   static constexpr int kEpi = kV + kVStages * kTile;  // softmax -> epilogue hand-off slots
   static constexpr int kBar = kEpi + 5 * 1024;
-  static constexpr int kBytes = kBar + 512;  // barriers, TMEM slot, flags, item ring
+  static constexpr int kLv = kBar + 512;  // after the barriers, TMEM slot, flags, item ring
+  static constexpr int kBytes = kLv + 4 * kMaxLevels;  // the scheduler's level table
   static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1 KB
   static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
   __host__ __device__ static constexpr int q(int side) { return kQ + side * kTile; }
@@ -217,6 +225,36 @@ __device__ __forceinline__ void tile_keys(const Item& I, int j, bool fused, int&
   }
 }
 
+// Query tokens [t0, t0 + qn) and length L of sequence s; false when it has
+// no query tokens or its metadata is out of range (bad).
+__device__ __forceinline__ bool seq_rows(const AttnArgs& a, int s, int& t0, int& qn, int& L,
+                                         bool& bad) {
+  t0 = __ldg(a.qsl + s);
+  qn = __ldg(a.qsl + s + 1) - t0;
+  L = __ldg(a.seq_lens + s);
+  bad = false;
+  if (qn <= 0) return false;
+  if (L < qn || L > (a.max_blocks << a.bs_log2) || qn > a.max_query_len || L > a.max_seq_len ||
+      t0 < 0 || t0 + qn > a.num_tokens) {
+    bad = true;
+    return false;
+  }
+  return true;
+}
+
+// Cost levels of prefill sequence sp's token tiles: tile t has level lo + t
+// (t < nt); pk_last: the last tile is packed (at most 64 tokens, group of
+// four heads).  Every level is at most ceil(max_seq_len / 128) + 1.
+__device__ __forceinline__ bool seq_levels(const AttnArgs& a, int sp, int& lo, int& nt,
+                                           bool& pk_last, bool& bad) {
+  int t0, qn, L;
+  if (!seq_rows(a, a.num_decode + sp, t0, qn, L, bad)) return false;
+  lo = (L - qn + kN - 1) / kN + 1;
+  nt = (qn + kM - 1) / kM;
+  pk_last = qn - (nt - 1) * kM <= kM / 2 && a.group % 4 == 0;
+  return true;
+}
+
 // Work slot e -> item.  Slots enumerate (cost level from max_level down to 1,
 // sequence, kv head, head pair); the sequence's tile at that level is
 // t = level - 1 - ceil(c / 128); a slot whose tile does not exist is empty.
@@ -233,16 +271,8 @@ __device__ bool decode_item(const AttnArgs& a, int e, int pairs, int max_level, 
   const int hk = rest / pairs;
   const int p = rest - hk * pairs;
   const int s = a.num_decode + sp;
-  const int t0 = __ldg(a.qsl + s);
-  const int qn = __ldg(a.qsl + s + 1) - t0;
-  const int L = __ldg(a.seq_lens + s);
-  bad = false;
-  if (qn <= 0) return false;
-  if (L < qn || L > (a.max_blocks << a.bs_log2) || qn > a.max_query_len || L > a.max_seq_len ||
-      t0 < 0 || t0 + qn > a.num_tokens) {
-    bad = true;
-    return false;
-  }
+  int t0, qn, L;
+  if (!seq_rows(a, s, t0, qn, L, bad)) return false;
   const int level = max_level - z;
   const int tile = level - 1 - (L - qn + kN - 1) / kN;
   if (tile < 0 || tile >= (qn + kM - 1) / kM) return false;
@@ -354,6 +384,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     *epi_total = INT_MAX;
     fence_barrier_init();
   }
+  if (!kCasc && warp == kSchedWarp && lane < a.num_seqs - a.num_decode) {
+    // the scheduler's first reads: the first prefill sequences' metadata
+    prefetch_l1(a.qsl + a.num_decode + lane);
+    prefetch_l1(a.qsl + a.num_decode + lane + 1);
+    prefetch_l1(a.seq_lens + a.num_decode + lane);
+  }
   if (threadIdx.x == 32 * kProducerWarp) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
@@ -438,57 +474,175 @@ __global__ void __launch_bounds__(kThreads, 1)
   regs_decrease<kProducerRegs>();
   if (warp == kSchedWarp) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0) {
-      int q_issued = 0;
-      for (int it = 0;; ++it) {
-        Item I;
-        I.n = 0;
-        while (true) {
-          const int e = static_cast<int>(atomicAdd(a.sched, 1u));
-          if (e >= total_slots) break;
-          bool bad;
-          if constexpr (kCasc) {
-            bad = false;
-            if (decode_item_casc(a, e, I)) break;
-          } else {
-            if (decode_item<kFused>(a, e, pairs, max_level, I, bad)) break;
+    // Dense work list: the global counter numbers only the items that exist,
+    // in slot order (cost level from the top, sequence, kv head, head pair),
+    // so every draw yields an item.  The warp first tabulates, per level z,
+    // lv[z] = the number of items at levels <= z (a difference array over
+    // each sequence's level range, summed twice); draw d then lies at level
+    // z, the smallest with lv[z] >= total - d, and is the (lv[z] - total + d)-th
+    // item of that level, found by a scan over the sequences.  With too many
+    // levels for the table, the counter walks the slots and skips empty ones.
+    constexpr unsigned kAll = 0xffffffffu;
+    int* lv = reinterpret_cast<int*>(sgen + Ly::kLv);
+    const int S_pre = a.num_seqs - a.num_decode;
+    const int M = a.hkv * pairs;            // items of one sequence at one level
+    const int Mp = a.hkv * (a.group >> 2);  // the same, packed tile
+    const bool dense = !kCasc && max_level + 2 <= kMaxLevels;
+    int total_items = 0;
+    if (dense) {
+      for (int z = lane; z < max_level + 2; z += 32) lv[z] = 0;
+      __syncwarp();
+      for (int sp = lane; sp < S_pre; sp += 32) {
+        int lo, nt;
+        bool pkl, bad;
+        if (seq_levels(a, sp, lo, nt, pkl, bad)) {
+          atomicAdd(lv + lo, M);
+          atomicAdd(lv + lo + nt, -M);
+          if (pkl) {
+            atomicAdd(lv + lo + nt - 1, Mp - M);
+            atomicAdd(lv + lo + nt, M - Mp);
           }
-          if (bad) flag_error(a.err, PA_DEV_BAD_LEN);
+        } else if (bad) {
+          flag_error(a.err, PA_DEV_BAD_LEN);
         }
-        const int slot = it & 1;
-        if (it >= 2 && !wait(bItemEmpty0 + slot, (it >> 1) - 1)) break;
-        ring[slot] = I;  // published by the releasing arrive below
-        mbar_arrive(BAR(bItemFull0 + slot));  // release: the entry is visible to waiters
-        if (I.n <= 0) break;
-        // Q of this item, into the Q buffers the previous item has finished with
-        if (it > 0 && !wait(bQFree, it - 1)) break;
-        const bool hasB = I.h[1] >= 0;
-        mbar_expect_tx(BAR(bQFull), Ly::kTile * (hasB ? 2 : 1));
-        if constexpr (kCasc) {
-          // a tile's rows come g at a time: the g query heads of kv head hk
-          // of one decode token (tm_q is [tokens, heads, D] here, box g heads);
-          // rows past the last sequence read an out-of-range token (zeros)
-          for (int sd = 0; sd < (hasB ? 2 : 1); ++sd) {
-            const uint32_t qdst = base + Ly::q(sd);
-            for (int rb = 0; rb < kM; rb += a.group) {
-              const int seq = (I.h[sd] * kM + rb) / a.group;
-              int t0 = seq < a.num_decode ? __ldg(a.qsl + seq) : a.num_tokens;
-              if (t0 < 0 || t0 >= a.num_tokens) t0 = a.num_tokens;
-#pragma unroll
-              for (int hf = 0; hf < Ly::kHalves; ++hf)
-                tma_load_3d(qdst + hf * Ly::kHalf + rb * 128, &tm_q, hf * 64, I.hk * a.group, t0,
-                            BAR(bQFull));
-            }
-          }
-        } else {
-          q_copy(I);
-        }
-        q_issued = it + 1;
       }
-      // drain: the last Q copy has landed before the CTA exits (each earlier
-      // one was consumed before the next was issued)
-      if (q_issued > 0) mbar_wait(BAR(bQFull), (q_issued - 1) & 1, kWaitNs);
+      __syncwarp();
+      int run1 = 0, run2 = 0;  // items at the levels so far; their running sum
+      for (int z0 = 0; z0 <= max_level; z0 += 32) {
+        const int z = z0 + lane;
+        int v = z <= max_level ? lv[z] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(kAll, v, o);
+          if (lane >= o) v += u;
+        }
+        int w = run1 + v;  // items at level z
+        run1 += __shfl_sync(kAll, v, 31);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(kAll, w, o);
+          if (lane >= o) w += u;
+        }
+        if (z <= max_level) lv[z] = run2 + w;
+        run2 += __shfl_sync(kAll, w, 31);
+      }
+      __syncwarp();
+      total_items = lv[max_level];
     }
+    // Slot of the d-th item of the dense list (every lane; -1: not found,
+    // which only metadata changing under the kernel could cause).
+    auto dense_slot = [&](int d) -> int {
+      const int u = total_items - d;
+      int zl = 1, zh = max_level;
+      while (zl < zh) {
+        const int mid = (zl + zh) >> 1;
+        if (lv[mid] >= u) zh = mid;
+        else zl = mid + 1;
+      }
+      const int z = zl;
+      const int k = lv[z] - u;
+      int acc = 0;
+      for (int s0 = 0; s0 < S_pre; s0 += 32) {
+        const int sp = s0 + lane;
+        int m = 0;
+        bool pk = false;
+        if (sp < S_pre) {
+          int lo, nt;
+          bool pkl, bad;
+          if (seq_levels(a, sp, lo, nt, pkl, bad) && z >= lo && z < lo + nt) {
+            pk = pkl && z == lo + nt - 1;
+            m = pk ? Mp : M;
+          }
+        }
+        int incl = m;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u2 = __shfl_up_sync(kAll, incl, o);
+          if (lane >= o) incl += u2;
+        }
+        const int tot = __shfl_sync(kAll, incl, 31);
+        if (k < acc + tot) {
+          const int src = __ffs(__ballot_sync(kAll, k < acc + incl)) - 1;
+          const int r = k - acc - __shfl_sync(kAll, incl - m, src);
+          const int mult = __shfl_sync(kAll, static_cast<int>(pk), src) ? (a.group >> 2) : pairs;
+          return ((max_level - z) * S_pre + s0 + src) * M + (r / mult) * pairs + r % mult;
+        }
+        acc += tot;
+      }
+      return -1;
+    };
+    // The next item of this CTA (every lane; I.n = 0: none left).  The first
+    // draw of CTA b is number b; the counter numbers the draws after the
+    // first wave.
+    bool first = true;
+    auto draw = [&](Item& I) {
+      I.n = 0;
+      while (true) {
+        unsigned e0 = 0;
+        if (first) e0 = blockIdx.x;
+        else if (lane == 0) e0 = gridDim.x + atomicAdd(a.sched, 1u);
+        first = false;
+        const int e = static_cast<int>(__shfl_sync(kAll, e0, 0));
+        bool bad = false;
+        if constexpr (kCasc) {
+          if (e >= total_slots) return;
+          if (decode_item_casc(a, e, I)) return;
+        } else if (dense) {
+          if (e >= total_items) return;
+          const int slot = dense_slot(e);
+          if (slot >= 0 && decode_item<kFused>(a, slot, pairs, max_level, I, bad)) return;
+        } else {
+          if (e >= total_slots) return;
+          if (decode_item<kFused>(a, e, pairs, max_level, I, bad)) return;
+          if (bad && lane == 0) flag_error(a.err, PA_DEV_BAD_LEN);
+        }
+      }
+    };
+    int q_issued = 0;
+    for (int it = 0;; ++it) {
+      Item I;
+      draw(I);
+      int stop = 0;
+      if (lane == 0) {
+        const int slot = it & 1;
+        if (it >= 2 && !wait(bItemEmpty0 + slot, (it >> 1) - 1)) {
+          stop = 1;
+        } else {
+          ring[slot] = I;  // published by the releasing arrive below
+          mbar_arrive(BAR(bItemFull0 + slot));  // release: the entry is visible to waiters
+          // Q of this item, into the Q buffers the previous item has finished with
+          if (I.n <= 0 || (it > 0 && !wait(bQFree, it - 1))) stop = 1;
+        }
+        if (!stop) {
+          const bool hasB = I.h[1] >= 0;
+          mbar_expect_tx(BAR(bQFull), Ly::kTile * (hasB ? 2 : 1));
+          if constexpr (kCasc) {
+            // a tile's rows come g at a time: the g query heads of kv head hk
+            // of one decode token (tm_q is [tokens, heads, D] here, box g heads);
+            // rows past the last sequence read an out-of-range token (zeros)
+            for (int sd = 0; sd < (hasB ? 2 : 1); ++sd) {
+              const uint32_t qdst = base + Ly::q(sd);
+              for (int rb = 0; rb < kM; rb += a.group) {
+                const int seq = (I.h[sd] * kM + rb) / a.group;
+                int t0 = seq < a.num_decode ? __ldg(a.qsl + seq) : a.num_tokens;
+                if (t0 < 0 || t0 >= a.num_tokens) t0 = a.num_tokens;
+#pragma unroll
+                for (int hf = 0; hf < Ly::kHalves; ++hf)
+                  tma_load_3d(qdst + hf * Ly::kHalf + rb * 128, &tm_q, hf * 64, I.hk * a.group,
+                              t0, BAR(bQFull));
+              }
+            }
+          } else {
+            q_copy(I);
+          }
+          q_issued = it + 1;
+        }
+      }
+      if (__shfl_sync(kAll, stop, 0)) break;
+    }
+    // drain: the last Q copy has landed before the CTA exits (each earlier
+    // one was consumed before the next was issued)
+    if (lane == 0 && q_issued > 0) mbar_wait(BAR(bQFull), (q_issued - 1) & 1, kWaitNs);
     __syncwarp();
   } else if (warp == kProducerWarp || warp == kVWarp) {
     // ------------------------------------------------------------ producers
