@@ -93,8 +93,9 @@ int pa_write_kv(const void* k, const void* v, int64_t k_stride_t, int64_t v_stri
 
 /*
  * pa_attention_workspace_size — bytes of scratch pa_attention needs: a
- * 256-byte header (the prefill kernel's work-queue counter, zeroed by each
- * call) followed by the split-KV decode partials (fp32 running max, sum and
+ * 256-byte header (the prefill kernel's work-queue counter, which that
+ * kernel tags per launch and resets itself, so no call zeroes it) followed by the
+ * split-KV decode partials (fp32 running max, sum and
  * weighted value per split, sequence and query head) when the decode rows are
  * split.  Never 0.  Depends on the current device's SM count; query it on the
  * device that will run the call.

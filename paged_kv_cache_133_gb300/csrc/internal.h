@@ -43,10 +43,13 @@ struct AttnArgs {
   int nsplit;    // grid splits = ceil(max_seq_len / part)
   float* ws_o;   // [nsplit, num_decode, hq, head_dim]
   float* ws_ml;  // [nsplit, num_decode, hq, 2]
-  // prefill work queue: a counter in the workspace header, zeroed per call
-  // (by the prefill launch, or before it when sched_zeroed)
-  unsigned int* sched;
-  bool sched_zeroed;
+  // Prefill work queue: a 64-bit word at the start of the workspace header,
+  // (launch tag << 32 | number of draws after the first wave).  The launch
+  // sets sched_tag (never 0, new for every launch); a word holding another
+  // tag is reset by the kernel itself and the kernel leaves it at (tag, 0),
+  // so the header needs no zeroing between calls.
+  unsigned long long* sched;
+  uint32_t sched_tag;
   // cap on the persistent prefill grid (0: one CTA per SM)
   int max_ctas;
   // Fused scatter for the prefill rows (null k_new: none).  The tensor-core

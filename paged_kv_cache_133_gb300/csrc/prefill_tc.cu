@@ -81,6 +81,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -223,6 +224,35 @@ __device__ __forceinline__ void tile_keys(const Item& I, int j, bool fused, int&
     key0 = j * kN;
     key_end = min(key0 + kN, fused ? I.c : I.kv_end);
   }
+}
+
+// Next count from a (tag << 32 | count) word of the work queue.  A word that
+// holds another launch's tag, or a count no draw of this launch can reach
+// (bound), is reset by the first CTA that manages to: it reads the word and
+// swaps exactly what it read for (tag, 1), taking 0.  A CTA adds to a stale
+// word at most once (its first try, which is the common case's only atomic),
+// so the swaps cannot be kept failing by other CTAs' additions for long.
+// False after many lost swaps (the caller reports it).
+__device__ bool tagged_take(unsigned long long* w, uint32_t tag, uint32_t bound, uint32_t& n) {
+  const unsigned long long mine = static_cast<unsigned long long>(tag) << 32;
+  auto fresh = [&](unsigned long long v) {
+    return (v >> 32) == tag && static_cast<uint32_t>(v) < bound;
+  };
+  unsigned long long v = atomicAdd(w, 1ull);
+  for (int tries = 0; tries < 4096; ++tries) {
+    if (fresh(v)) {
+      n = static_cast<uint32_t>(v);
+      return true;
+    }
+    const unsigned long long cur = atomicOr(w, 0ull);  // read
+    if (fresh(cur)) {
+      v = atomicAdd(w, 1ull);
+    } else if (atomicCAS(w, cur, mine | 1ull) == cur) {
+      n = 0;
+      return true;
+    }
+  }
+  return false;
 }
 
 // Query tokens [t0, t0 + qn) and length L of sequence s; false when it has
@@ -488,6 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int M = a.hkv * pairs;            // items of one sequence at one level
     const int Mp = a.hkv * (a.group >> 2);  // the same, packed tile
     const bool dense = !kCasc && max_level + 2 <= kMaxLevels;
+    // The work counter as this launch finds it; read now, used after the
+    // table is built (see below).
+    unsigned long long seen = 0;
+    if (lane == 0) seen = atomicOr(a.sched, 0ull);
     int total_items = 0;
     if (dense) {
       for (int z = lane; z < max_level + 2; z += 32) lv[z] = 0;
@@ -572,15 +606,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       return -1;
     };
     // The next item of this CTA (every lane; I.n = 0: none left).  The first
-    // draw of CTA b is number b; the counter numbers the draws after the
-    // first wave.
+    // draw of CTA b is number b; the work counter numbers the draws after the
+    // first wave.  Every CTA with a first item draws until a draw comes back
+    // past the list (T numbers: items, or slots), so a launch makes exactly T
+    // counted draws whatever the timing, and the CTA that draws count T - 1
+    // made the last one: it leaves the word at (tag, 0), so that a replay of
+    // the same launch (a CUDA graph keeps its arguments) starts from 0.
     bool first = true;
+    const uint32_t T = static_cast<uint32_t>(dense ? total_items : total_slots);
+    // A counter left by another launch is reset before the first wave
+    // draws from it: each CTA swaps exactly the stale value it read for
+    // (tag, 0), so only the first swap takes effect and none can undo a draw.
+    // A CTA that draws before any swap has landed resets it in tagged_take.
+    if (lane == 0 && !((seen >> 32) == a.sched_tag && static_cast<uint32_t>(seen) < T))
+      atomicCAS(a.sched, seen, static_cast<unsigned long long>(a.sched_tag) << 32);
     auto draw = [&](Item& I) {
       I.n = 0;
       while (true) {
         unsigned e0 = 0;
-        if (first) e0 = blockIdx.x;
-        else if (lane == 0) e0 = gridDim.x + atomicAdd(a.sched, 1u);
+        if (first) {
+          e0 = blockIdx.x;
+        } else if (lane == 0) {
+          uint32_t n;
+          if (tagged_take(a.sched, a.sched_tag, T, n)) {
+            e0 = gridDim.x + n;
+            if (n == T - 1) atomicExch(a.sched, static_cast<unsigned long long>(a.sched_tag) << 32);
+          } else {
+            flag_error(a.err, PA_DEV_TIMEOUT);
+            e0 = 0x7fffffffu;  // no more items for this CTA
+          }
+        }
         first = false;
         const int e = static_cast<int>(__shfl_sync(kAll, e0, 0));
         bool bad = false;
@@ -599,9 +654,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     int q_issued = 0;
+    bool drawn_out = false;  // a draw came back past the list
     for (int it = 0;; ++it) {
       Item I;
       draw(I);
+      drawn_out = I.n <= 0;
       int stop = 0;
       if (lane == 0) {
         const int slot = it & 1;
@@ -639,6 +696,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (__shfl_sync(kAll, stop, 0)) break;
+    }
+    // A CTA that gave up mid-way still draws to the end of the list (without
+    // running the items), which keeps the count of draws at T.
+    while (!drawn_out) {
+      Item I;
+      draw(I);
+      drawn_out = I.n <= 0;
     }
     // drain: the last Q copy has landed before the CTA exits (each earlier
     // one was consumed before the next was issued)
@@ -1248,6 +1312,17 @@ bool encode_new(CUtensorMap* m, const void* ptr, int64_t stride, const AttnArgs&
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A new work-queue tag for each launch (never 0, so that a zeroed header
+// reads as another launch's).
+uint32_t next_sched_tag() {
+  static std::atomic<uint32_t> tag{0};
+  uint32_t t;
+  do {
+    t = tag.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  } while (t == 0u);
+  return t;
+}
+
 // Highest cost level: every visible key range is at most max_seq_len keys.
 int max_level_of(const AttnArgs& a) { return (a.max_seq_len + kN - 1) / kN + 1; }
 
@@ -1269,7 +1344,9 @@ cudaError_t allow_smem(K kernel, int bytes, bool (&done)[64]) {
 }
 
 template <int D, bool kFused>
-cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_tc_d(const AttnArgs& args, cudaStream_t st) {
+  AttnArgs a = args;
+  a.sched_tag = next_sched_tag();
   using Ly = PpLayout<D>;
   static bool done[2][64] = {};
   auto kernel = a.wait_ns ? prefill_tc_kernel<D, kFused, false, true> : prefill_tc_kernel<D, kFused>;
@@ -1288,8 +1365,6 @@ cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t st) {
   if (a.max_ctas > 0 && a.max_ctas < sms) sms = a.max_ctas;  // SMs left to a concurrent decode
   const int grid = total < sms ? total : sms;
   if (grid <= 0) return cudaSuccess;
-  e = a.sched_zeroed ? cudaSuccess : cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
-  if (e != cudaSuccess) return e;
   count_launch();
   const int max_level = max_level_of(a);
   e = launch_prio(kernel, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
@@ -1303,7 +1378,9 @@ int64_t cascade_tc_slots(const AttnArgs& a) {
 }
 
 template <int D>
-cudaError_t launch_casc_d(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_casc_d(const AttnArgs& args, cudaStream_t st) {
+  AttnArgs a = args;
+  a.sched_tag = next_sched_tag();
   using Ly = PpLayout<D>;
   static bool done[2][64] = {};
   auto kernel = a.wait_ns ? prefill_tc_kernel<D, false, true, true> : prefill_tc_kernel<D, false, true>;
@@ -1320,8 +1397,6 @@ cudaError_t launch_casc_d(const AttnArgs& a, cudaStream_t st) {
   const int sms = device_num_sms();
   const int grid = total < sms ? total : sms;
   if (grid <= 0) return cudaSuccess;
-  e = cudaMemsetAsync(a.sched, 0, sizeof(unsigned int), st);
-  if (e != cudaSuccess) return e;
   count_launch();
   e = launch_prio(kernel, dim3(grid), dim3(kThreads), Ly::kAlloc, st,
                   a.has_priority, a.priority, mq, mk, mv, mo, mkn, mvn, mq64, a, total, 1);

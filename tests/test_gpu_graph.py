@@ -72,10 +72,11 @@ def test_graph_replay_matches_eager(lay, fused):
         step(replay)
     torch.cuda.synchronize()
     for _ in range(3):
+        replay.fill_(float("nan"))  # every replay must write every row again
         graph.replay()
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert torch.equal(replay.view(torch.int16), eager.view(torch.int16))
     assert int(err.item()) == 0
-    assert torch.equal(replay.view(torch.int16), eager.view(torch.int16))
     assert torch.equal(g["k_cache"].view(torch.int16), kc1.view(torch.int16))
     assert torch.equal(g["v_cache"].view(torch.int16), vc1.view(torch.int16))
     assert np.isfinite(H.f64(replay)).all()
@@ -119,3 +120,60 @@ def test_cascade_graph_replay_matches_eager(g8):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(replay.view(torch.int16), eager.view(torch.int16))
+
+
+def test_work_queue_needs_no_zeroing():
+    # The persistent prefill kernel draws items from two words in the
+    # workspace header that the host never zeroes: each launch tags them, a
+    # word holding another launch's tag (or any bytes) is reset by the kernel,
+    # and the last CTA leaves them ready for a replay of the same launch.  Two
+    # captured steps with more items than CTAs share one workspace and replay
+    # alternately, some replays after the header was overwritten with ones,
+    # and an eager call follows a clobbered header too.
+    lays = [workloads.custom_layout("qa", [0] * 6, [700, 500, 300, 129, 64, 1000], 32, 8, 128,
+                                    16, 400, 21),
+            workloads.custom_layout("qb", [200, 0, 900], [640, 1500, 77], 32, 8, 128, 16, 600, 22)]
+    need = max(pa.workspace_size(0, l.num_q_heads, l.num_kv_heads, l.head_dim, l.max_seq_len)
+               for l in lays)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    runs = []
+    for lay in lays:
+        g = workloads.make_tensors(lay, seed=13, device=DEV)
+        md = H.device_meta(lay, DEV)
+        pa.write_kv(g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"], err=err)
+        out = torch.full_like(g["q"], float("nan"))
+
+        def attn(lay=lay, g=g, md=md, out=out):
+            pa.attention(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"], md["bt"],
+                         num_decode_seqs=0, max_query_len=lay.max_query_len,
+                         max_seq_len=lay.max_seq_len, scale=lay.scale, out=out, workspace=ws,
+                         err=err)
+
+        attn()
+        torch.cuda.synchronize()
+        runs.append((attn, out, out.clone()))
+    graphs = []
+    for attn, _, _ in runs:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            attn()
+        torch.cuda.synchronize()
+        graphs.append(gr)
+    for rep in range(4):
+        for (attn, out, expect), gr in zip(runs, graphs):
+            if rep % 2:
+                ws[:64].fill_(255)
+            out.fill_(float("nan"))
+            gr.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), expect.view(torch.int16)), rep
+    attn, out, expect = runs[1]
+    ws[:64].fill_(255)
+    out.fill_(float("nan"))
+    attn()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), expect.view(torch.int16))
+    assert int(err.item()) == 0
