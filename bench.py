@@ -221,6 +221,15 @@ class Step:
         if attn_events is not None:
             attn_events[1].record()
 
+    def attention(self):
+        """The step's attention call alone (the cache already holds the new
+        tokens' K/V)."""
+        pa, lay, g, md = self.pa, self.lay, self.g, self.md
+        pa.attention(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"], md["bt"],
+                     num_decode_seqs=lay.num_decode_seqs, max_query_len=lay.max_query_len,
+                     max_seq_len=lay.max_seq_len, scale=lay.scale, out=self.out,
+                     workspace=self.ws, err=self.err)
+
 
 def _barrier(dist_on):
     if dist_on:
@@ -495,8 +504,9 @@ def secondary(dev, steps, warmup, peaks):
     res = {}
     lay = workloads.config_layout(3, 0)
     st = Step(lay, dev)
-    ms, attn_ms, _ = time_device(st, steps, warmup, False)
+    ms, attn_eager, _ = time_device(st, steps, warmup, False)
     msg = time_graph(st)
+    attn_ms = time_call_graph(st.attention, dev)
     fl = attention_flops(lay, np.arange(lay.num_seqs))
     tf = fl / (attn_ms * 1e-3) / 1e12
     del st
@@ -505,13 +515,19 @@ def secondary(dev, steps, warmup, peaks):
     res["prefill"] = {"workload": "16 prompts (log-uniform 16..2048, sum 8192), 32q/8kv, D 128, bs 16",
                       "fused_ms_per_step": msf, "fused_TFLOP/s_per_step": fl / (msf * 1e-3) / 1e12,
                       "metric": "prefill TFLOP/s", "value": tf, "ms_attention": attn_ms,
+                      "ms_attention_eager": attn_eager,
+                      "timing": "ms_attention: the attention launch alone, 8 launches in one CUDA "
+                                "graph, each after a 256 MB write that flushes L2, minus the same "
+                                "graph without the launches; ms_attention_eager: events around "
+                                "eager calls, which include host launch gaps",
                       "ms_per_step": ms, "graph_ms_per_step": msg, "flops": fl,
                       "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16"],
                                    "unit": "TFLOP/s", "frac": tf / peaks["bf16"]}}
     del st
     lay = workloads.config_layout(6, 0)
     st = Step(lay, dev)
-    ms6, attn6, _ = time_device(st, steps, warmup, False)
+    ms6, attn6_eager, _ = time_device(st, steps, warmup, False)
+    attn6 = time_call_graph(st.attention, dev)
     fl6 = attention_flops(lay, np.arange(lay.num_seqs))
     tf6 = fl6 / (attn6 * 1e-3) / 1e12
     del st
@@ -520,6 +536,7 @@ def secondary(dev, steps, warmup, peaks):
     res["prefix"] = {"workload": "32 prefix-cache hits: cached U[1024,8192], new chunks U[64,512], 32q/8kv, D 128, bs 16",
                      "fused_ms_per_step": msf6, "fused_TFLOP/s_per_step": fl6 / (msf6 * 1e-3) / 1e12,
                      "metric": "prefix-cached prefill TFLOP/s", "value": tf6, "ms_attention": attn6,
+                     "ms_attention_eager": attn6_eager,
                      "ms_per_step": ms6, "flops": fl6,
                      "roofline": {"bound": "tensor", "achieved": tf6, "peak": peaks["bf16"],
                                   "unit": "TFLOP/s", "frac": tf6 / peaks["bf16"]}}
@@ -527,6 +544,7 @@ def secondary(dev, steps, warmup, peaks):
     lay = workloads.config_layout(4, 0)
     st = Step(lay, dev)
     ms, attn_ms, _ = time_device(st, steps, warmup, False)
+    attn4g = time_call_graph(st.attention, dev)
     dec = np.arange(lay.num_decode_seqs)
     pre = np.arange(lay.num_decode_seqs, lay.num_seqs)
     t_dec = decode_kernel_bytes(lay, dec) / (peaks["hbm"] * 1e9)
@@ -560,6 +578,8 @@ def secondary(dev, steps, warmup, peaks):
                     "graph_ms_per_step": ms4g,
                     "additive_roofline_ms": t_star * 1e3, "frac": t_star * 1e3 / ms,
                     "overlap_roofline_ms": t_over * 1e3, "overlap_frac": t_over * 1e3 / ms,
+                    "ms_attention_graph": attn4g,
+                    "attention_overlap_frac": t_over * 1e3 / attn4g,
                     "note": "the decode and prefill kernels run side by side on split SMs, so "
                             "max(decode bytes / HBM peak, prefill FLOPs / bf16 peak) bounds the "
                             "step from below; the additive bound is the serial one"}
@@ -568,6 +588,48 @@ def secondary(dev, steps, warmup, peaks):
     res["kv_copy"] = kv_copy_leg(dev, peaks)
     res["worked"] = worked_leg(dev)
     return res
+
+
+def time_call_graph(fn, dev, calls=8, replays=5):
+    """Device time (ms) of one `fn` launch with no host gaps and a cold L2.
+    Two CUDA graphs are captured: `calls` times (write a 256 MB buffer, twice
+    the L2; call fn), and the same writes alone.  Each is replayed between
+    events; the launch time is the difference per call (best replay of each)."""
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+
+    def capture(with_fn):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(calls):
+                flush.fill_(i & 255)
+                if with_fn:
+                    fn()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        return graph
+
+    def best_ms(graph):
+        best = float("inf")
+        for _ in range(replays):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    g_both, g_flush = capture(True), capture(False)
+    t = (best_ms(g_both) - best_ms(g_flush)) / calls
+    del g_both, g_flush, flush
+    return t
 
 
 def _graph_us(fns, launches):

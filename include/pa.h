@@ -41,7 +41,7 @@
  *   PA_CASCADE_IMPL=mma    pa_attention_cascade's prefix pass on the mma.sync
  *                          kernel instead of the tcgen05 one.
  *   PA_MIXED_DECODE_SMS=n  SMs left to the decode rows while a mixed step's
- *                          prefill runs beside them (default 49 % of the SMs).
+ *                          prefill runs beside them (default 84 of every 152 SMs).
  */
 #ifndef PA_H_
 #define PA_H_
