@@ -2,7 +2,8 @@
 // chunked prefill), on mma.sync tensor-core tiles.  This is the general path:
 // any head_dim in {64, 128}, any power-of-two block size, any GQA ratio.  The
 // tcgen05 kernel (prefill_tc.cu) takes over whenever it supports the call
-// (scale > 0, 16-byte aligned rows); PA_PREFILL_IMPL=mma forces this one.
+// (scale > 0, 16-byte aligned q rows, 32-byte aligned output rows);
+// PA_PREFILL_IMPL=mma forces this one.
 //
 // Work unit: one CTA per (64-row query tile, kv head, sequence).  The rows of
 // a sequence's tile are (new token i, query head of the kv head's group)

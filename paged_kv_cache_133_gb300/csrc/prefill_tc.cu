@@ -1173,11 +1173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               f2_split(f2_mul(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2));
           w[e] = pack_bf16(on.x, on.y);
         }
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 16);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
+        if (live) st_global_v8(orow + cc * 16, w);  // 32 bytes, one instruction
       }
       return true;
     };
@@ -1424,7 +1420,9 @@ bool prefill_tc_supported(const AttnArgs& a) {
   if (env && strcmp(env, "mma") == 0) return false;
   if (a.head_dim != 64 && a.head_dim != 128) return false;
   if (!(a.scale_log2 > 0.f)) return false;  // the row maximum is taken before scaling
-  if ((a.q_stride * 2) % 16 != 0 || (a.out_stride * 2) % 16 != 0) return false;
+  // 16-byte rows for TMA; the epilogue stores 32 bytes at a time
+  if ((a.q_stride * 2) % 16 != 0 || (a.out_stride * 2) % 32 != 0) return false;
+  if (reinterpret_cast<uintptr_t>(a.out) & 31u) return false;
   if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k_cache) |
        reinterpret_cast<uintptr_t>(a.v_cache) | reinterpret_cast<uintptr_t>(a.out)) & 15u)
     return false;
