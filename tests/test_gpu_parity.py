@@ -292,6 +292,31 @@ def test_prefill_kernels_match_oracle(lay, prefill_impl):
     H.assert_close(H.f64(out), H.oracle_full(lay, ts), f"{lay.name}/{prefill_impl}")
 
 
+@pytest.mark.parametrize("pad", [8, 16], ids=["16B_rows", "32B_rows"])
+def test_prefill_output_with_padded_rows(pad):
+    # An output whose token stride carries `pad` extra elements.  Rows that
+    # are 16- but not 32-byte aligned (pad 8) take the general kernel, since
+    # the tensor-core epilogue stores 32 bytes at a time; pad 16 keeps the
+    # tensor-core path.  Both must write only their own rows.
+    lay = _prefill_cases()[0]
+    ts = workloads.make_tensors(lay, seed=9, poison=True)
+    g = {k: v.to(DEV) for k, v in ts.items()}
+    T, hq, d = g["q"].shape
+    buf = torch.full((T, hq * d + pad), float("nan"), dtype=torch.bfloat16, device=DEV)
+    if pad == 16:  # rows at the start of each padded row: 32-byte aligned
+        out = buf[:, :hq * d].view(T, hq, d)
+        rest = buf[:, hq * d:]
+    else:  # rows 16 bytes into each padded row: 16- but not 32-byte aligned
+        out = torch.as_strided(buf, (T, hq, d), (hq * d + pad, d, 1), storage_offset=pad)
+        rest = buf[:, :pad]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    H.run_step(lay, g, H.device_meta(lay, DEV), err=err, out=out)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    H.assert_close(H.f64(out), H.oracle_full(lay, ts), f"padded rows {pad}")
+    assert torch.isnan(rest.float()).all(), "a kernel wrote outside the output rows"
+
+
 @pytest.mark.parametrize("cfg", [3, 4, 6])
 def test_prefill_full_size_both_kernels_agree(cfg, monkeypatch):
     # the tensor-core and the general kernel on the same full-size batch
