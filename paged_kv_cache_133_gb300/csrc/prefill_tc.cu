@@ -109,6 +109,12 @@ constexpr int kProducerRegs = 64;
 constexpr int kEpiRegs = 48;
 static_assert(2 * kSoftmaxRegs + kProducerRegs + kEpiRegs == 4 * 65536 / kThreads,
               "the warpgroups' register limits must add up to the launch's");
+// With the fused scatter the producers carry more state: 8 more registers
+// for them, 8 fewer for the epilogue.
+constexpr int kProducerRegsFused = 72;
+constexpr int kEpiRegsFused = 40;
+static_assert(2 * kSoftmaxRegs + kProducerRegsFused + kEpiRegsFused == 4 * 65536 / kThreads,
+              "the warpgroups' register limits must add up to the launch's");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -501,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Each warpgroup's register limit is set at the top of its own branch, so
   // that the compiler allocates each role's code within its own limit.
   if (warp >= kProducerWarp && warp < kEpiWarp0) {
-  regs_decrease<kProducerRegs>();
+  regs_decrease<kFused ? kProducerRegsFused : kProducerRegs>();
   if (warp == kSchedWarp) {
     // ------------------------------------------------------------ scheduler
     // Dense work list: the global counter numbers only the items that exist,
@@ -1106,7 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // bf16 and stores it straight to the output, 16 bytes at a time (these
     // warps are off the softmax's critical path, so they need no staging
     // buffer).  The shared-prefix mode writes fp32 partials (O, m, l).
-    regs_decrease<kEpiRegs>();
+    regs_decrease<kFused ? kEpiRegsFused : kEpiRegs>();
     const int q4 = warp - kEpiWarp0;
     const int r = q4 * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
