@@ -292,6 +292,48 @@ def test_prefill_kernels_match_oracle(lay, prefill_impl):
     H.assert_close(H.f64(out), H.oracle_full(lay, ts), f"{lay.name}/{prefill_impl}")
 
 
+def test_prefill_slot_walk_is_bitwise_identical():
+    # Beyond 2046 cost levels (max_seq_len above 261,760) the scheduler walks
+    # every (level, sequence, head pair) slot and skips the empty ones instead
+    # of using its dense item table.  max_seq_len is only an upper bound, so
+    # a small batch passed with max_seq_len 300,000 takes that path: about
+    # 37,500 slots, nearly all empty, so every CTA's first slot is empty and
+    # the draws come from the work counter.  The same items run in the same
+    # order, so the output is bit for bit the dense list's, eagerly and
+    # replayed from a CUDA graph (the counter's reset at the last draw
+    # covers slots too).
+    lay = _prefill_cases()[0]
+    g = workloads.make_tensors(lay, seed=5, device=DEV)
+    md = H.device_meta(lay, DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa.write_kv(g["k"], g["v"], g["k_cache"], g["v_cache"], md["slots"], err=err)
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device=DEV)
+
+    def attn(out, max_seq_len):
+        pa.attention(g["q"], g["k_cache"], g["v_cache"], md["qsl"], md["seq_lens"], md["bt"],
+                     num_decode_seqs=0, max_query_len=lay.max_query_len,
+                     max_seq_len=max_seq_len, scale=lay.scale, out=out, workspace=ws, err=err)
+
+    expect = torch.empty_like(g["q"])
+    attn(expect, lay.max_seq_len)
+    out = torch.full_like(g["q"], float("nan"))
+    attn(out, 300_000)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), expect.view(torch.int16))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        attn(out, 300_000)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), expect.view(torch.int16))
+    assert int(err.item()) == 0
+
+
 @pytest.mark.parametrize("pad", [8, 16], ids=["16B_rows", "32B_rows"])
 def test_prefill_output_with_padded_rows(pad):
     # An output whose token stride carries `pad` extra elements.  Rows that
