@@ -640,7 +640,7 @@ def time_call_graph(fn, dev, calls=8, replays=5):
 
 def _graph_us(fns, launches):
     """Microseconds per launch of `launches` calls cycling through `fns`,
-    captured in one CUDA graph (no host launch gaps) and replayed."""
+    captured in one CUDA graph (no host launch gaps); best of 5 replays."""
     import torch
     for f in fns:
         f()
@@ -655,7 +655,7 @@ def _graph_us(fns, launches):
     graph.replay()
     torch.cuda.synchronize()
     best = float("inf")
-    for _ in range(3):
+    for _ in range(5):
         a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         graph.replay()
